@@ -1,0 +1,393 @@
+#!/usr/bin/env python
+"""Benchmark of one MoE layer (DeepSeek-V3 shape) on GB300.
+
+One step = the whole hot path over one batch: router GEMM, top-k, dispatch
+(histogram, scan, permute), routed gate/up and down grouped GEMMs, shared
+expert, combine -- one ``moe_layer`` call of the C library.  Inputs are
+seeded synthetic tensors of the workload's shapes, resident in HBM.
+
+  python bench.py [--gpus N --steps K --warmup W] [--config dsv3_prefill]
+  python bench.py --impl reference ...   # the CPU oracle on host cores
+
+With N > 1 (launched by torchrun) every rank runs an independent replica of
+the layer on its own GPU (the path has no exchange step on one GPU); the
+reported time is the maximum over ranks and the value counts all ranks'
+tokens.  Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (DeepSeek-V3 shape)"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 512 << 20
+# our kernels per moe_layer call: router GEMM, top-k, count+scan, permute,
+# gate/up GEMM, down GEMM (routed), gate/up GEMM, down GEMM (shared), combine
+LAUNCHES_PER_STEP_SHARED = 9
+LAUNCHES_PER_STEP_NOSHARED = 7
+
+# DRAM traffic of the routed gate/up GEMM per launch, from an ncu capture of
+# the same kernel source (see profiles/); None when the source has changed.
+TRAFFIC = {"source_sha256": None, "bytes_per_launch_at_workload": {}}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return dict(hbm_gbs=j["hbm_gbs"], bf16=j["bf16_tflops"],
+                    bf16_sustained=j.get("bf16_tflops_sustained", j["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index: int):
+        self.proc = None
+        self.dev = dev_index
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            import torch
+            sel = str(self.dev)
+            try:
+                bus = torch.cuda.get_device_properties(self.dev).pci_bus_id
+                if bus:
+                    sel = bus
+            except Exception:
+                pass
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={sel}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is None:
+            return False
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle leg
+
+def oracle_sample(cfg, inp, n_tok, seed=0):
+    """Run the CPU oracle on n_tok sampled tokens; returns (seconds, tokens)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from combine_router_gemm_gb300 import inputs
+
+    npy = inputs.to_numpy
+    g = torch.Generator()
+    g.manual_seed(seed)
+    tok = torch.randperm(cfg.T, generator=g)[:n_tok].sort().values
+    x = npy(inp["x"][tok.to(inp["x"].device)])
+    fn = oracle.SIGMOID if cfg.score_fn == "sigmoid" else oracle.SOFTMAX
+    w = inp["_host"]
+    t0 = time.perf_counter()
+    oracle.moe_tokens(x, E=cfg.E, k=cfg.k, w13=w["w13"], w2=w["w2"], w_router=w["w_router"],
+                      bias=w["bias"], n_group=cfg.n_group, topk_group=cfg.topk_group,
+                      score_fn=fn, routed_scale=cfg.routed_scale, w13_sh=w["w13_sh"],
+                      w2_sh=w["w2_sh"], round_h=cfg.dtype == "bf16")
+    return time.perf_counter() - t0, n_tok
+
+
+def host_weights(inp):
+    from combine_router_gemm_gb300 import inputs
+    npy = inputs.to_numpy
+    return {k: npy(inp[k]) for k in ("w13", "w2", "w_router", "bias", "w13_sh", "w2_sh")}
+
+
+def cpu_baseline(cfg, inp, target_s=15.0):
+    import oracle
+    inp["_host"] = inp.get("_host") or host_weights(inp)
+    probe = 16
+    dt, _ = oracle_sample(cfg, inp, probe, seed=1)
+    n = int(max(probe, min(cfg.T, probe * target_s / max(dt, 1e-3))))
+    dt, n = oracle_sample(cfg, inp, n, seed=2)
+    return {"value": n / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} of {cfg.T} tokens of {cfg.name}, whole layer per token "
+                      f"(router, top-{cfg.k}, experts, shared expert), {dt:.1f} s"}
+
+
+def run_reference(args, cfg):
+    rank, local_rank, world = env_rank()
+    if rank != 0:
+        return 0
+    import torch
+
+    import oracle
+    from combine_router_gemm_gb300 import inputs
+    oracle.build()
+    dev = f"cuda:{local_rank}" if torch.cuda.is_available() else "cpu"
+    inp = inputs.make_inputs(cfg, seed=0, device=dev)
+    inp["_host"] = host_weights(inp)
+    # size one step's token sample so the whole run stays within a few minutes
+    dt, _ = oracle_sample(cfg, inp, 8, seed=99)
+    per_tok = dt / 8
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = max(1, min(cfg.T, int(budget / max(per_tok, 1e-6))))
+    for w in range(args.warmup):
+        oracle_sample(cfg, inp, n, seed=1000 + w)
+    total = 0.0
+    for s in range(args.steps):
+        dt, _ = oracle_sample(cfg, inp, n, seed=s)
+        total += dt
+    value = n * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(cfg, flushed=False),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{n} of {cfg.T} tokens per step of {cfg.name}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+
+def config_dict(cfg, flushed=True):
+    return {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "I": cfg.I,
+            "shared_I": cfg.shared_I, "routing": f"{cfg.score_fn}, {cfg.n_group} groups keep "
+            f"{cfg.topk_group}, scale {cfg.routed_scale}, bias {cfg.bias}",
+            "global_batch": cfg.T,
+            "l2": ("flushed between steps (512 MB write)" if flushed else "n/a (host)"),
+            "parallelism": "replicas (one independent layer per GPU)"}
+
+
+def kernel_source_sha():
+    p = os.path.join(ROOT, "combine_router_gemm_gb300", "csrc", "grouped_gemm_tc.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()
+
+
+def run_ours(args, cfg):
+    import torch
+    import torch.distributed as dist
+
+    rank, local_rank, world = env_rank()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    from combine_router_gemm_gb300 import binding as B
+    from combine_router_gemm_gb300 import build as build_mod
+    from combine_router_gemm_gb300 import inputs
+    build_mod.build()
+
+    pk = peaks()
+    inp = inputs.make_inputs(cfg, seed=0, device="cuda")
+    layer = B.MoELayer(inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"],
+                       inp["w2_sh"], B.cfg_from(cfg), cfg.T, overlap=not args.no_overlap)
+    x = inp["x"]
+    out = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device="cuda")
+    offs = torch.empty(cfg.E + 1, dtype=torch.int32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    warm = max(3, args.warmup)
+    for _ in range(warm):
+        layer.forward(x, out=out, offsets_out=offs)
+    rc, detail = B.moe_check_error(layer.ws)
+    if rc != B.OK:
+        raise RuntimeError(f"device error word {detail:#x} during warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(B.LAYER_EVENTS)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t_wall = time.perf_counter()
+        for s in range(K):
+            flush.zero_()
+            layer.forward(x, out=out, offsets_out=offs, stage_events=evs[s])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    rc, detail = B.moe_check_error(layer.ws)
+    if rc != B.OK:
+        raise RuntimeError(f"device error word {detail:#x} during the timed steps")
+
+    step_ms = [e[0].elapsed_time(e[-1]) for e in evs]
+    stage_ms = [statistics.fmean(e[i].elapsed_time(e[i + 1]) for e in evs)
+                for i in range(B.LAYER_EVENTS - 1)]
+    total_s = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+    value = cfg.T * K * world / total_s
+
+    # ---- algorithmic work per stage (bytes / flops per launch)
+    o = offs.cpu().numpy()
+    active = int((o[1:] - o[:-1] > 0).sum())
+    S, d, I, T, E = cfg.S, cfg.d, cfg.I, cfg.T, cfg.E
+    es = 2 if cfg.dtype == "bf16" else 4
+    gu_bytes = active * 2 * I * d * es + S * d * es + S * I * es
+    gu_flops = 2.0 * S * d * 2 * I
+    dn_bytes = active * d * I * es + S * I * es + S * d * 4
+    dn_flops = 2.0 * S * I * d
+    perm_bytes = T * d * es + S * d * es + S * 4 * 3 + S * 4
+    names = ["router", "topk", "dispatch", "gate_up_gemm", "down_gemm", "shared_wait+combine"]
+    stages = {n: {"ms": round(m, 4)} for n, m in zip(names, stage_ms)}
+
+    def bw(b, ms):
+        return b / (ms * 1e-3) / 1e9
+
+    def tf(f, ms):
+        return f / (ms * 1e-3) / 1e12
+
+    stages["dispatch"].update(GBps=round(bw(perm_bytes, stage_ms[2]), 1),
+                              frac_hbm=round(bw(perm_bytes, stage_ms[2]) / pk["hbm_gbs"], 4))
+    for key, b, f, ms in (("gate_up_gemm", gu_bytes, gu_flops, stage_ms[3]),
+                          ("down_gemm", dn_bytes, dn_flops, stage_ms[4])):
+        stages[key].update(GBps=round(bw(b, ms), 1), TFLOPs=round(tf(f, ms), 1),
+                           frac_hbm=round(bw(b, ms) / pk["hbm_gbs"], 4),
+                           frac_bf16=round(tf(f, ms) / pk["bf16_sustained"], 4))
+    ridge = pk["bf16_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    ai = gu_flops / gu_bytes
+    ms = stage_ms[3]
+    traffic = None
+    if TRAFFIC["source_sha256"] == kernel_source_sha():
+        traffic = TRAFFIC["bytes_per_launch_at_workload"].get(cfg.name)
+    if ai < ridge:
+        roof = {"bound": "hbm", "achieved": round(bw(gu_bytes, ms), 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(bw(gu_bytes, ms) / pk["hbm_gbs"], 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(tf(gu_flops, ms), 1),
+                "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
+                "frac": round(tf(gu_flops, ms) / pk["bf16_sustained"], 4)}
+    roof.update(traffic=traffic, kernel="grouped_gemm_tc gate/up+SwiGLU (routed)",
+                algorithmic_bytes=gu_bytes, algorithmic_flops=gu_flops,
+                arithmetic_intensity=round(ai, 1), peak_source=pk["source"],
+                launch_ms=round(ms, 4))
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.empty((T, d), dtype=x.dtype, pin_memory=True)
+        xh.copy_(x)
+        oh = torch.empty((T, d), dtype=torch.float32, pin_memory=True)
+        xd = torch.empty_like(x)
+        ne = args.e2e_steps
+        for _ in range(3):
+            xd.copy_(xh, non_blocking=True)
+            layer.forward(xd, out=out)
+            oh.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        es_, ee_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        es_.record()
+        for _ in range(ne):
+            xd.copy_(xh, non_blocking=True)
+            layer.forward(xd, out=out)
+            oh.copy_(out, non_blocking=True)
+        ee_.record()
+        torch.cuda.synchronize()
+        e_s = es_.elapsed_time(ee_) / 1e3
+        if world > 1:
+            t = torch.tensor([e_s], device="cuda", dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_s = float(t.item())
+        e2e = {"value": T * ne * world / e_s, "unit": UNIT, "h2d_bytes_per_step": T * d * x.element_size(),
+               "d2h_bytes_per_step": T * d * 4, "steps": ne}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, inp)
+
+    if rank == 0:
+        launches = (LAUNCHES_PER_STEP_SHARED if cfg.shared_I else LAUNCHES_PER_STEP_NOSHARED) * K
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": warm, "ms_per_step": 1e3 * total_s / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+            "config": config_dict(cfg), "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clk.summary(), "stages": stages,
+            "active_experts": active, "wall_s_timed": round(t_wall, 3),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="dsv3_prefill")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true", help="shared expert on the main stream")
+    args = ap.parse_args()
+    from combine_router_gemm_gb300 import inputs
+    cfg = inputs.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

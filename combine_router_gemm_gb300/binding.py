@@ -1,0 +1,300 @@
+"""Thin Python binding of ``include/moe.h`` (argument marshalling only).
+
+Each function takes torch tensors, checks that they are contiguous CUDA
+tensors of the expected dtype, passes their device pointers, sizes and the
+current CUDA stream to the C entry point of the same name, and raises
+``MoEError`` on a non-OK status.  All computation happens in the CUDA library
+``libmoe_gb300.so``; there is no fallback of any kind.  If the library is
+missing, loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_INPUT = range(7)
+F32, BF16 = 0, 1
+SOFTMAX, SIGMOID = 0, 1
+
+# every symbol include/moe.h declares
+SYMBOLS = ("moe_status_string", "moe_version", "moe_route_from_scores", "moe_route",
+           "moe_dispatch_workspace_size", "moe_dispatch", "moe_grouped_ffn_workspace_size",
+           "moe_grouped_ffn", "moe_combine", "moe_layer_workspace_size", "moe_layer",
+           "moe_check_error")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class RouteCfg(ctypes.Structure):
+    _fields_ = [("num_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("n_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
+                ("score_fn", ctypes.c_int32), ("routed_scale", ctypes.c_float)]
+
+
+class LayerArgs(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("w_router", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("w13", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("w13_sh", ctypes.c_void_p),
+                ("w2_sh", ctypes.c_void_p), ("T", ctypes.c_int32), ("d", ctypes.c_int32),
+                ("I", ctypes.c_int32), ("I_sh", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("route", RouteCfg), ("scores_out", ctypes.c_void_p),
+                ("topk_idx_out", ctypes.c_void_p), ("topk_w_out", ctypes.c_void_p),
+                ("offsets_out", ctypes.c_void_p), ("stage_events", ctypes.c_void_p)]
+
+LAYER_EVENTS = 7
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                           "(run __graft_entry__.build() or combine_router_gemm_gb300.build)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.moe_status_string.argtypes = [i32]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    lib.moe_version.argtypes = []
+    lib.moe_version.restype = i32
+    lib.moe_route_from_scores.argtypes = [P, P, i32, ctypes.POINTER(RouteCfg), P, P, P]
+    lib.moe_route_from_scores.restype = i32
+    lib.moe_route.argtypes = [P, i32, P, P, i32, i32, ctypes.POINTER(RouteCfg), P, P, P, P]
+    lib.moe_route.restype = i32
+    lib.moe_dispatch_workspace_size.argtypes = [i32, i32, i32]
+    lib.moe_dispatch_workspace_size.restype = sz
+    lib.moe_dispatch.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, sz, P]
+    lib.moe_dispatch.restype = i32
+    lib.moe_grouped_ffn_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.moe_grouped_ffn_workspace_size.restype = sz
+    lib.moe_grouped_ffn.argtypes = [P, P, i32, i32, i32, i32, P, P, i32, P, P, sz, P]
+    lib.moe_grouped_ffn.restype = i32
+    lib.moe_combine.argtypes = [P, P, P, P, i32, i32, i32, P, P]
+    lib.moe_combine.restype = i32
+    lib.moe_layer_workspace_size.argtypes = [ctypes.POINTER(LayerArgs)]
+    lib.moe_layer_workspace_size.restype = sz
+    lib.moe_layer.argtypes = [ctypes.POINTER(LayerArgs), P, P, sz, P, P]
+    lib.moe_layer.restype = i32
+    lib.moe_check_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.moe_check_error.restype = i32
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().moe_status_string(int(status)).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != OK:
+        raise MoEError(rc, where)
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def route_cfg(E: int, k: int, n_group: int = 1, topk_group: int = 1, score_fn: int = SOFTMAX,
+              routed_scale: float = 1.0) -> RouteCfg:
+    return RouteCfg(E, k, n_group, topk_group, score_fn, routed_scale)
+
+
+def cfg_from(c) -> RouteCfg:
+    """RouteCfg from a workload description with E, k, n_group, topk_group, score_fn, routed_scale."""
+    return route_cfg(c.E, c.k, c.n_group, c.topk_group,
+                     SIGMOID if c.score_fn == "sigmoid" else SOFTMAX, c.routed_scale)
+
+
+# ---------------------------------------------------------------- entry points
+
+def moe_route_from_scores(scores, bias, cfg: RouteCfg, topk_idx, topk_w, stream=None):
+    T = scores.shape[0]
+    rc = load().moe_route_from_scores(_ptr(scores, torch.float32, "scores"),
+                                      _ptr(bias, torch.float32, "bias"), T, ctypes.byref(cfg),
+                                      _ptr(topk_idx, torch.int32, "topk_idx"),
+                                      _ptr(topk_w, torch.float32, "topk_w"), _stream(stream))
+    _check(rc, "moe_route_from_scores")
+
+
+def moe_route(x, w_router, bias, cfg: RouteCfg, scores, topk_idx, topk_w, stream=None):
+    T, d = x.shape
+    rc = load().moe_route(_ptr(x, None, "x"), _dtype_code(x), _ptr(w_router, torch.float32, "w_router"),
+                          _ptr(bias, torch.float32, "bias"), T, d, ctypes.byref(cfg),
+                          _ptr(scores, torch.float32, "scores"),
+                          _ptr(topk_idx, torch.int32, "topk_idx"),
+                          _ptr(topk_w, torch.float32, "topk_w"), _stream(stream))
+    _check(rc, "moe_route")
+
+
+def moe_dispatch_workspace_size(T: int, k: int, E: int) -> int:
+    return load().moe_dispatch_workspace_size(T, k, E)
+
+
+def moe_dispatch(topk_idx, x, E: int, counts, offsets, slot_to_row, row_to_token, x_perm, ws,
+                 stream=None):
+    T, k = topk_idx.shape
+    d = x.shape[1] if x is not None else 8
+    dt = _dtype_code(x) if x is not None else BF16
+    rc = load().moe_dispatch(_ptr(topk_idx, torch.int32, "topk_idx"), _ptr(x, None, "x"), dt, T, d,
+                             k, E, _ptr(counts, torch.int32, "counts"),
+                             _ptr(offsets, torch.int32, "offsets"),
+                             _ptr(slot_to_row, torch.int32, "slot_to_row"),
+                             _ptr(row_to_token, torch.int32, "row_to_token"),
+                             _ptr(x_perm, None, "x_perm"), _ptr(ws, None, "ws"),
+                             ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "moe_dispatch")
+
+
+def moe_grouped_ffn_workspace_size(rows: int, d: int, I: int, dtype: int) -> int:
+    return load().moe_grouped_ffn_workspace_size(rows, d, I, dtype)
+
+
+def moe_grouped_ffn(x_perm, offsets, w13, w2, y_perm, ws, stream=None):
+    rows, d = x_perm.shape
+    E, I = w2.shape[0], w2.shape[2]
+    rc = load().moe_grouped_ffn(_ptr(x_perm, None, "x_perm"), _ptr(offsets, torch.int32, "offsets"),
+                                E, rows, d, I, _ptr(w13, x_perm.dtype, "w13"),
+                                _ptr(w2, x_perm.dtype, "w2"), _dtype_code(x_perm),
+                                _ptr(y_perm, torch.float32, "y_perm"), _ptr(ws, None, "ws"),
+                                ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "moe_grouped_ffn")
+
+
+def moe_combine(y_perm, slot_to_row, topk_w, shared, out, stream=None):
+    T, k = topk_w.shape
+    d = out.shape[1]
+    rc = load().moe_combine(_ptr(y_perm, torch.float32, "y_perm"),
+                            _ptr(slot_to_row, torch.int32, "slot_to_row"),
+                            _ptr(topk_w, torch.float32, "topk_w"),
+                            _ptr(shared, torch.float32, "shared"), T, k, d,
+                            _ptr(out, torch.float32, "out"), _stream(stream))
+    _check(rc, "moe_combine")
+
+
+def layer_args(x, w_router, bias, w13, w2, w13_sh, w2_sh, cfg: RouteCfg, scores_out=None,
+               topk_idx_out=None, topk_w_out=None, offsets_out=None,
+               stage_events=None) -> LayerArgs:
+    """``stage_events``: None or a list of LAYER_EVENTS torch.cuda.Event (kept
+    alive by the caller), recorded by the library at the stage boundaries."""
+    T, d = x.shape
+    I = w2.shape[2]
+    I_sh = w2_sh.shape[1] if w2_sh is not None else 0
+    return LayerArgs(_ptr(x, None, "x"), _ptr(w_router, torch.float32, "w_router"),
+                     _ptr(bias, torch.float32, "bias"), _ptr(w13, x.dtype, "w13"),
+                     _ptr(w2, x.dtype, "w2"), _ptr(w13_sh, x.dtype, "w13_sh"),
+                     _ptr(w2_sh, x.dtype, "w2_sh"), T, d, I, I_sh, _dtype_code(x), cfg,
+                     _ptr(scores_out, torch.float32, "scores_out"),
+                     _ptr(topk_idx_out, torch.int32, "topk_idx_out"),
+                     _ptr(topk_w_out, torch.float32, "topk_w_out"),
+                     _ptr(offsets_out, torch.int32, "offsets_out"), _events(stage_events))
+
+
+_event_arrays = {}
+
+
+def _events(evs):
+    """Host array of cudaEvent_t handles for torch events (cached per list)."""
+    if evs is None:
+        return None
+    if len(evs) != LAYER_EVENTS:
+        raise ValueError(f"need {LAYER_EVENTS} events")
+    key = tuple(id(e) for e in evs)
+    arr = _event_arrays.get(key)
+    if arr is None:
+        for e in evs:  # torch creates the CUDA event lazily on first record
+            if e.cuda_event == 0:
+                e.record()
+        arr = (ctypes.c_void_p * LAYER_EVENTS)(*[e.cuda_event for e in evs])
+        _event_arrays[key] = (arr, evs)
+    else:
+        arr = arr[0]
+    return ctypes.cast(arr, ctypes.c_void_p).value
+
+
+def moe_layer_workspace_size(args: LayerArgs) -> int:
+    n = load().moe_layer_workspace_size(ctypes.byref(args))
+    if n == 0:
+        raise MoEError(ERR_INVALID_ARG, "moe_layer_workspace_size")
+    return n
+
+
+def moe_layer(args: LayerArgs, out, ws, stream=None, stream2=None):
+    s2 = stream2.cuda_stream if stream2 is not None else None
+    rc = load().moe_layer(ctypes.byref(args), _ptr(out, torch.float32, "out"), _ptr(ws, None, "ws"),
+                          ws.numel() * ws.element_size(), _stream(stream), s2)
+    _check(rc, "moe_layer")
+
+
+def moe_check_error(ws, stream=None) -> tuple[int, int]:
+    detail = ctypes.c_uint32(0)
+    rc = load().moe_check_error(_ptr(ws, None, "ws"), _stream(stream), ctypes.byref(detail))
+    return rc, detail.value
+
+
+# ---------------------------------------------------------------- convenience
+
+class MoELayer:
+    """Holds the weights of one layer plus a workspace; ``forward(x)`` -> out fp32 [T,d].
+
+    ``x`` must have the token count the layer was built for (workspace size
+    depends on it).  Allocation happens only here, in PyTorch, never in the
+    library.
+    """
+
+    def __init__(self, w_router, bias, w13, w2, w13_sh, w2_sh, cfg: RouteCfg, T: int,
+                 overlap: bool = True):
+        self.w = dict(w_router=w_router, bias=bias, w13=w13, w2=w2, w13_sh=w13_sh, w2_sh=w2_sh)
+        self.cfg = cfg
+        self.T = T
+        dev = w13.device
+        d = w13.shape[2]
+        probe = torch.empty((T, d), dtype=w13.dtype, device=dev)
+        self.ws_bytes = moe_layer_workspace_size(self._args(probe))
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.stream2 = torch.cuda.Stream(device=dev) if overlap and w13_sh is not None else None
+
+    def _args(self, x, **outs):
+        w = self.w
+        return layer_args(x, w["w_router"], w["bias"], w["w13"], w["w2"], w["w13_sh"],
+                          w["w2_sh"], self.cfg, **outs)
+
+    def forward(self, x, out=None, **outs):
+        if x.shape[0] != self.T:
+            raise ValueError(f"layer built for T={self.T}, got {x.shape[0]}")
+        if out is None:
+            out = torch.empty((x.shape[0], x.shape[1]), dtype=torch.float32, device=x.device)
+        moe_layer(self._args(x, **outs), out, self.ws, stream2=self.stream2)
+        return out

@@ -1,0 +1,353 @@
+// api.cu -- the C entry points: argument checks, workspace layout, launches.
+//
+// Every check runs on the host before anything is enqueued; see moe.h for
+// the contract of each call.
+#include <math.h>
+
+#include <climits>
+
+#include "common.cuh"
+
+namespace moe_tc {
+int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
+                     const void* w13, const void* w2, float* y, void* h, uint32_t* err,
+                     cudaStream_t s, cudaEvent_t between = nullptr);
+}
+namespace moe_f32 {
+int grouped_ffn_f32(const float* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
+                    const float* w13, const float* w2, float* y, float* h, const uint32_t* err,
+                    cudaStream_t s);
+}
+
+namespace moe_host {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int launch_status() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return 1;
+    return n;
+}
+
+}  // namespace moe_host
+
+namespace {
+
+constexpr size_t ERR_BYTES = 256;  // error word region at the start of a workspace
+
+size_t al(size_t v) { return (v + 255) / 256 * 256; }
+
+bool dtype_ok(int dt) { return dt == MOE_F32 || dt == MOE_BF16; }
+size_t esize(int dt) { return dt == MOE_BF16 ? 2 : 4; }
+
+int check_cfg(const moe_route_cfg* c) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    const int E = c->num_experts, k = c->top_k, g = c->n_group, tg = c->topk_group;
+    if (E < 1 || k < 1 || g < 1 || tg < 1) return MOE_ERR_INVALID_ARG;
+    if (c->score_fn != MOE_SCORE_SOFTMAX && c->score_fn != MOE_SCORE_SIGMOID)
+        return MOE_ERR_INVALID_ARG;
+    if (!isfinite(c->routed_scale)) return MOE_ERR_INVALID_ARG;
+    if (E % g != 0 || tg > g) return MOE_ERR_INVALID_ARG;
+    if (g > 1 && E / g < 2) return MOE_ERR_INVALID_ARG;
+    const int eligible = g > 1 ? tg * (E / g) : E;
+    if (k > eligible) return MOE_ERR_INVALID_ARG;
+    if (E > 1024 || k > 32 || g > 32) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+int check_dims(long long T, int d, int k) {
+    if (T < 0 || d < 8 || d % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (T * (long long)k > INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+size_t ffn_ws(int rows, int d, int I, int dtype) {
+    (void)d;
+    return ERR_BYTES + al((size_t)rows * I * esize(dtype));
+}
+
+int run_ffn(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
+            const void* w13, const void* w2, int dtype, float* y, void* h, uint32_t* err,
+            cudaStream_t s, cudaEvent_t between = nullptr) {
+    if (rows == 0) {
+        if (between && cudaEventRecord(between, s) != cudaSuccess) return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    if (dtype == MOE_BF16)
+        return moe_tc::grouped_ffn_bf16(x_perm, offsets, E, rows, d, I, w13, w2, y, h, err, s,
+                                        between);
+    int rc = moe_f32::grouped_ffn_f32(static_cast<const float*>(x_perm), offsets, E, rows, d, I,
+                                      static_cast<const float*>(w13), static_cast<const float*>(w2),
+                                      y, static_cast<float*>(h), err, s);
+    if (rc == MOE_OK && between && cudaEventRecord(between, s) != cudaSuccess) rc = MOE_ERR_CUDA;
+    return rc;
+}
+
+struct LayerWs {
+    uint32_t* err;
+    float* scores;
+    int32_t* idx;
+    float* w;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* s2r;
+    int32_t* r2t;
+    void* xp;
+    float* yp;
+    void* h;
+    float* ysh;
+    void* hsh;
+    void* disp;
+    size_t total;
+};
+
+LayerWs carve_layer(const moe_layer_args* a, void* base) {
+    const int T = a->T, d = a->d, I = a->I, E = a->route.num_experts, k = a->route.top_k;
+    const size_t S = (size_t)T * k, es = esize(a->dtype);
+    char* p = static_cast<char*>(base);
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> void* {
+        void* r = p ? p + off : nullptr;
+        off += al(bytes);
+        return r;
+    };
+    LayerWs w;
+    w.err = static_cast<uint32_t*>(take(ERR_BYTES));
+    w.scores = a->scores_out ? a->scores_out : static_cast<float*>(take((size_t)T * E * 4));
+    w.idx = a->topk_idx_out ? a->topk_idx_out : static_cast<int32_t*>(take(S * 4));
+    w.w = a->topk_w_out ? a->topk_w_out : static_cast<float*>(take(S * 4));
+    w.counts = static_cast<int32_t*>(take((size_t)E * 4));
+    w.offsets = a->offsets_out ? a->offsets_out : static_cast<int32_t*>(take((size_t)(E + 1) * 4));
+    w.s2r = static_cast<int32_t*>(take(S * 4));
+    w.r2t = static_cast<int32_t*>(take(S * 4));
+    w.xp = take(S * d * es);
+    w.yp = static_cast<float*>(take(S * d * 4));
+    w.h = take(S * I * es);
+    const bool sh = a->w13_sh && a->w2_sh && a->I_sh > 0;
+    w.ysh = sh ? static_cast<float*>(take((size_t)T * d * 4)) : nullptr;
+    w.hsh = sh ? take((size_t)T * a->I_sh * es) : nullptr;
+    w.disp = take(moe_launch::dispatch_ws_bytes(T, k, E));
+    w.total = off;
+    return w;
+}
+
+int check_layer(const moe_layer_args* a) {
+    if (!a) return MOE_ERR_INVALID_ARG;
+    int rc = check_cfg(&a->route);
+    if (rc != MOE_OK) return rc;
+    if ((rc = check_dims(a->T, a->d, a->route.top_k)) != MOE_OK) return rc;
+    if (!dtype_ok(a->dtype) || a->I < 8 || a->I % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (!a->x || !a->w_router || !a->w13 || !a->w2) return MOE_ERR_INVALID_ARG;
+    if (!moe_host::aligned16(a->x) || !moe_host::aligned16(a->w_router) ||
+        !moe_host::aligned16(a->w13) || !moe_host::aligned16(a->w2))
+        return MOE_ERR_INVALID_ARG;
+    if (a->bias && a->route.score_fn == MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
+    const bool sh = a->w13_sh || a->w2_sh || a->I_sh;
+    if (sh) {
+        if (!a->w13_sh || !a->w2_sh || a->I_sh < 8 || a->I_sh % 8 != 0) return MOE_ERR_INVALID_ARG;
+        if (!moe_host::aligned16(a->w13_sh) || !moe_host::aligned16(a->w2_sh))
+            return MOE_ERR_INVALID_ARG;
+    }
+    const void* outs[] = {a->scores_out, a->topk_idx_out, a->topk_w_out, a->offsets_out};
+    for (const void* o : outs)
+        if (o && !moe_host::aligned16(o)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+        case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_TIMEOUT: return "a bounded device wait ran out";
+        case MOE_ERR_DEVICE_INPUT: return "inconsistent device-side input";
+        default: return "unknown status";
+    }
+}
+
+int moe_version(void) { return 100; }
+
+int moe_route_from_scores(const float* scores, const float* bias, int T, const moe_route_cfg* cfg,
+                          int32_t* topk_idx, float* topk_w, void* stream) {
+    int rc = check_cfg(cfg);
+    if (rc != MOE_OK) return rc;
+    if (T < 0 || !scores || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (bias && cfg->score_fn == MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    return moe_launch::topk(scores, bias, T, cfg, topk_idx, topk_w,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int moe_route(const void* x, int dtype, const float* w_router, const float* bias, int T, int d,
+              const moe_route_cfg* cfg, float* scores, int32_t* topk_idx, float* topk_w,
+              void* stream) {
+    int rc = check_cfg(cfg);
+    if (rc != MOE_OK) return rc;
+    if ((rc = check_dims(T, d, cfg->top_k)) != MOE_OK) return rc;
+    if (!dtype_ok(dtype) || !x || !w_router || !scores || !topk_idx || !topk_w)
+        return MOE_ERR_INVALID_ARG;
+    if (!moe_host::aligned16(x) || !moe_host::aligned16(w_router)) return MOE_ERR_INVALID_ARG;
+    if (bias && cfg->score_fn == MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = moe_launch::router_gemm(x, dtype, w_router, T, d, cfg->num_experts, cfg->score_fn, scores,
+                                 s);
+    if (rc != MOE_OK) return rc;
+    return moe_launch::topk(scores, bias, T, cfg, topk_idx, topk_w, s);
+}
+
+size_t moe_dispatch_workspace_size(int T, int k, int E) {
+    if (T < 0 || k < 1 || E < 1) return 0;
+    return ERR_BYTES + moe_launch::dispatch_ws_bytes(T, k, E);
+}
+
+int moe_dispatch(const int32_t* topk_idx, const void* x, int dtype, int T, int d, int k, int E,
+                 int32_t* counts, int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_token,
+                 void* x_perm, void* ws, size_t ws_bytes, void* stream) {
+    if (k < 1 || k > 32 || E < 1 || E > 1024) return E > 1024 ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
+    int rc = check_dims(T, d, k);
+    if (rc != MOE_OK) return rc;
+    if (!dtype_ok(dtype) || !topk_idx || !counts || !offsets || !slot_to_row || !row_to_token)
+        return MOE_ERR_INVALID_ARG;
+    if ((x_perm != nullptr) != (x != nullptr)) return MOE_ERR_INVALID_ARG;
+    if (x && (!moe_host::aligned16(x) || !moe_host::aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < moe_dispatch_workspace_size(T, k, E)) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t* err = static_cast<uint32_t*>(ws);
+    if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (T == 0) {
+        if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s) != cudaSuccess ||
+            cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    return moe_launch::dispatch(topk_idx, x, dtype, T, d, k, E, counts, offsets, slot_to_row,
+                                row_to_token, x_perm, static_cast<char*>(ws) + ERR_BYTES, err, s);
+}
+
+size_t moe_grouped_ffn_workspace_size(int rows, int d, int I, int dtype) {
+    if (rows < 0 || d < 1 || I < 1 || !dtype_ok(dtype)) return 0;
+    return ffn_ws(rows, d, I, dtype);
+}
+
+int moe_grouped_ffn(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
+                    const void* w13, const void* w2, int dtype, float* y_perm, void* ws,
+                    size_t ws_bytes, void* stream) {
+    if (E < 1 || rows < 0 || d < 8 || d % 8 || I < 8 || I % 8 || !dtype_ok(dtype))
+        return MOE_ERR_INVALID_ARG;
+    if (E > 1024) return MOE_ERR_UNSUPPORTED;
+    if (!x_perm || !offsets || !w13 || !w2 || !y_perm) return MOE_ERR_INVALID_ARG;
+    if (!moe_host::aligned16(x_perm) || !moe_host::aligned16(w13) || !moe_host::aligned16(w2) ||
+        !moe_host::aligned16(y_perm))
+        return MOE_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < ffn_ws(rows, d, I, dtype)) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t* err = static_cast<uint32_t*>(ws);
+    if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    return run_ffn(x_perm, offsets, E, rows, d, I, w13, w2, dtype, y_perm,
+                   static_cast<char*>(ws) + ERR_BYTES, err, s);
+}
+
+int moe_combine(const float* y_perm, const int32_t* slot_to_row, const float* topk_w,
+                const float* shared, int T, int k, int d, float* out, void* stream) {
+    if (T < 0 || k < 1 || d < 4 || d % 4) return MOE_ERR_INVALID_ARG;
+    if (k > 32) return MOE_ERR_UNSUPPORTED;
+    if (!y_perm || !slot_to_row || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+    if (!moe_host::aligned16(y_perm) || !moe_host::aligned16(out) ||
+        (shared && !moe_host::aligned16(shared)))
+        return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    return moe_launch::combine(y_perm, slot_to_row, topk_w, shared, T, k, d, out, nullptr,
+                               static_cast<cudaStream_t>(stream));
+}
+
+size_t moe_layer_workspace_size(const moe_layer_args* a) {
+    if (check_layer(a) != MOE_OK) return 0;
+    return carve_layer(a, nullptr).total;
+}
+
+int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, void* stream,
+              void* stream2) {
+    int rc = check_layer(a);
+    if (rc != MOE_OK) return rc;
+    if (!out || !moe_host::aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if (!ws || !moe_host::aligned16(ws) || ws_bytes < carve_layer(a, nullptr).total)
+        return MOE_ERR_WORKSPACE;
+    const LayerWs w = carve_layer(a, ws);
+    const int T = a->T, d = a->d, I = a->I, E = a->route.num_experts, k = a->route.top_k;
+    cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+    cudaStream_t s1 = static_cast<cudaStream_t>(stream2);
+    if (cudaMemsetAsync(w.err, 0, sizeof(uint32_t), s0) != cudaSuccess) return MOE_ERR_CUDA;
+    if (T == 0) return MOE_OK;
+    const bool sh = w.ysh != nullptr;
+    cudaEvent_t stage[MOE_LAYER_EVENTS] = {};
+    if (a->stage_events)
+        for (int i = 0; i < MOE_LAYER_EVENTS; ++i) stage[i] = static_cast<cudaEvent_t>(a->stage_events[i]);
+    auto mark = [&](int i) {
+        if (rc == MOE_OK && stage[i] && cudaEventRecord(stage[i], s0) != cudaSuccess) rc = MOE_ERR_CUDA;
+    };
+    mark(0);
+    cudaEvent_t ev_start = nullptr, ev_shared = nullptr;
+    const bool overlap = sh && s1 && s1 != s0;
+    if (overlap) {
+        if (cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ev_shared, cudaEventDisableTiming) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (cudaEventRecord(ev_start, s0) != cudaSuccess ||
+            cudaStreamWaitEvent(s1, ev_start, 0) != cudaSuccess)
+            rc = MOE_ERR_CUDA;
+        if (rc == MOE_OK)
+            rc = run_ffn(a->x, nullptr, 1, T, d, a->I_sh, a->w13_sh, a->w2_sh, a->dtype, w.ysh, w.hsh,
+                         w.err, s1);
+        if (rc == MOE_OK && cudaEventRecord(ev_shared, s1) != cudaSuccess) rc = MOE_ERR_CUDA;
+    }
+    if (rc == MOE_OK)
+        rc = moe_launch::router_gemm(a->x, a->dtype, a->w_router, T, d, E, a->route.score_fn,
+                                     w.scores, s0);
+    mark(1);
+    if (rc == MOE_OK) rc = moe_launch::topk(w.scores, a->bias, T, &a->route, w.idx, w.w, s0);
+    mark(2);
+    if (rc == MOE_OK)
+        rc = moe_launch::dispatch(w.idx, a->x, a->dtype, T, d, k, E, w.counts, w.offsets, w.s2r,
+                                  w.r2t, w.xp, w.disp, w.err, s0);
+    mark(3);
+    if (rc == MOE_OK)
+        rc = run_ffn(w.xp, w.offsets, E, T * k, d, I, a->w13, a->w2, a->dtype, w.yp, w.h, w.err, s0,
+                     stage[4]);
+    mark(5);
+    if (rc == MOE_OK && sh && !overlap)
+        rc = run_ffn(a->x, nullptr, 1, T, d, a->I_sh, a->w13_sh, a->w2_sh, a->dtype, w.ysh, w.hsh,
+                     w.err, s0);
+    if (rc == MOE_OK && overlap && cudaStreamWaitEvent(s0, ev_shared, 0) != cudaSuccess)
+        rc = MOE_ERR_CUDA;
+    if (rc == MOE_OK)
+        rc = moe_launch::combine(w.yp, w.s2r, w.w, w.ysh, T, k, d, out, w.err, s0);
+    mark(6);
+    if (ev_start) cudaEventDestroy(ev_start);
+    if (ev_shared) cudaEventDestroy(ev_shared);
+    return rc;
+}
+
+int moe_check_error(void* ws, void* stream, uint32_t* detail) {
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (v && cudaMemset(ws, 0, sizeof v) != cudaSuccess) return MOE_ERR_CUDA;
+    if (detail) *detail = v;
+    if (v & moe::ERR_TIMEOUT_MASK) return MOE_ERR_TIMEOUT;
+    if (v) return MOE_ERR_DEVICE_INPUT;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// combine.cu -- gate-weighted combine of the expert outputs.
+//
+// The pages ("CUCo: An Agentic Framework for Compute and Communication
+// Co-design", Table 4 row "MoE Dispatch/Combine") bring each token's expert
+// results back to it; on one GPU that is a weighted gather:
+//   out[t,:] = sum_{j<k} w[t,j] * y[slot_to_row[t*k+j], :]  (+ shared[t,:]),
+// summed in slot order in fp32.  One block per token; each thread owns a few
+// 16-byte column chunks and issues the k row loads of a chunk back to back.
+#include "common.cuh"
+
+namespace {
+
+constexpr int CB_THREADS = 256;
+constexpr int CB_MAXK = 32;
+
+__global__ void __launch_bounds__(CB_THREADS) combine_kernel(
+    const float4* __restrict__ y, const int32_t* __restrict__ slot_to_row,
+    const float* __restrict__ w, const float4* __restrict__ shared, int T, int k, int d4,
+    float4* __restrict__ out, const uint32_t* err) {
+    __shared__ int s_row[CB_MAXK];
+    __shared__ float s_w[CB_MAXK];
+    __shared__ int s_skip;
+    const int t = blockIdx.x;
+    const int rows = T * k;
+    if (threadIdx.x == 0) s_skip = moe::read_error(err) != 0;
+    if (threadIdx.x < k) {
+        int r = slot_to_row[(size_t)t * k + threadIdx.x];
+        s_row[threadIdx.x] = (r >= 0 && r < rows) ? r : -1;
+        s_w[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
+    }
+    __syncthreads();
+    if (s_skip) return;
+    for (int v = threadIdx.x; v < d4; v += CB_THREADS) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const int r = s_row[j];
+            const float wj = s_w[j];
+            if (r < 0) {  // an index outside y: make the damage visible
+                acc = make_float4(__int_as_float(0x7fc00000), 0.f, 0.f, 0.f);
+                continue;
+            }
+            const float4 yv = __ldcs(y + (size_t)r * d4 + v);
+            acc.x = fmaf(wj, yv.x, acc.x);
+            acc.y = fmaf(wj, yv.y, acc.y);
+            acc.z = fmaf(wj, yv.z, acc.z);
+            acc.w = fmaf(wj, yv.w, acc.w);
+        }
+        if (shared) {
+            const float4 sv = __ldcs(shared + (size_t)t * d4 + v);
+            acc.x += sv.x;
+            acc.y += sv.y;
+            acc.z += sv.z;
+            acc.w += sv.w;
+        }
+        out[(size_t)t * d4 + v] = acc;
+    }
+}
+
+}  // namespace
+
+namespace moe_launch {
+
+int combine(const float* y, const int32_t* slot_to_row, const float* w, const float* shared, int T,
+            int k, int d, float* out, const uint32_t* err, cudaStream_t s) {
+    if (k > CB_MAXK) return MOE_ERR_UNSUPPORTED;
+    combine_kernel<<<T, CB_THREADS, 0, s>>>(
+        reinterpret_cast<const float4*>(y), slot_to_row, w, reinterpret_cast<const float4*>(shared),
+        T, k, d / 4, reinterpret_cast<float4*>(out), err);
+    return moe_host::launch_status();
+}
+
+}  // namespace moe_launch

@@ -1,0 +1,76 @@
+// common.cuh -- shared device helpers of the MoE CUDA library (sm_103a).
+//
+// Error word: a uint32 in device memory.  Kernels OR in a code when a bounded
+// wait runs out or a device-side input is inconsistent, then stop early.
+// Consumers of earlier stages read it on entry and skip their work if set.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// error-word bits
+constexpr uint32_t ERR_TIMEOUT_SCAN = 1u << 0;
+constexpr uint32_t ERR_TIMEOUT_PIPE = 1u << 1;
+constexpr uint32_t ERR_BAD_INDEX = 1u << 8;
+constexpr uint32_t ERR_BAD_OFFSETS = 1u << 9;
+constexpr uint32_t ERR_TIMEOUT_MASK = 0xffu;
+
+// a bounded wait gives up after this many nanoseconds of %globaltimer
+constexpr uint64_t WAIT_LIMIT_NS = 1000ull * 1000ull * 1000ull;
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void raise_error(uint32_t* err, uint32_t code) {
+    if (err) atomicOr(err, code);
+}
+
+__device__ __forceinline__ uint32_t read_error(const uint32_t* err) {
+    return err ? *(volatile const uint32_t*)err : 0u;
+}
+
+__device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+}  // namespace moe
+
+// ---- host-side helpers shared by the entry points (defined in api.cu) ------
+namespace moe_host {
+bool aligned16(const void* p);
+int launch_status();  // MOE_OK or MOE_ERR_CUDA after a launch
+int num_sms();
+}  // namespace moe_host
+
+// ---- internal launchers (one per kernel family), used by api.cu -----------
+namespace moe_launch {
+int router_gemm(const void* x, int dtype, const float* w_router, int T, int d, int E, int score_fn,
+                float* scores, cudaStream_t s);
+int topk(const float* scores, const float* bias, int T, const moe_route_cfg* cfg, int32_t* idx,
+         float* w, cudaStream_t s);
+size_t dispatch_ws_bytes(int T, int k, int E);
+int dispatch(const int32_t* idx, const void* x, int dtype, int T, int d, int k, int E, int32_t* counts,
+             int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_token, void* x_perm, void* ws,
+             uint32_t* err, cudaStream_t s);
+size_t ffn_ws_bytes(int rows, int I, int dtype);
+int grouped_ffn(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
+                const void* w13, const void* w2, int dtype, float* y, void* h_ws, uint32_t* err,
+                cudaStream_t s);
+int combine(const float* y, const int32_t* slot_to_row, const float* w, const float* shared, int T,
+            int k, int d, float* out, const uint32_t* err, cudaStream_t s);
+}  // namespace moe_launch

@@ -1,0 +1,561 @@
+// grouped_gemm_tc.cu -- per-expert SwiGLU FFN as tcgen05 grouped GEMMs (bf16).
+//
+// The pages ("CUCo: An Agentic Framework for Compute and Communication
+// Co-design", abstract and Table 4 row "MoE Dispatch/Combine") put local expert
+// compute between dispatch and combine, and note padding overhead on
+// imbalanced loads.  Here every expert's rows form one exact, unpadded segment
+// [offsets[e], offsets[e+1]) of the permuted activations, and two persistent
+// kernels compute
+//   gate/up:  H[r, n] = bf16( silu(<x_r, W1_e[n]>) * <x_r, W3_e[n]> )
+//   down:     Y[r, n] = <H_r, W2_e[n]>                         (fp32)
+// with fp32 accumulation in tensor memory.
+//
+// Design (sm_103a):
+//  * Swap-AB: the MMA's M side (128) walks output features (weight rows), its
+//    N side walks tokens (16..256, rounded up to 16 per tile).  Small and
+//    ragged segments then cost N granularity 16 rather than a 128-row tile,
+//    and every weight tile of an expert is read once per 256 tokens.
+//  * One CTA per SM (persistent), 6 warps: warp 0 issues TMA loads, warp 1
+//    allocates tensor memory and issues tcgen05.mma from one thread, warps 2-5
+//    drain the accumulators (tcgen05.ld) and store.  Shared-memory stages are
+//    handed over with mbarriers; the accumulator is handed over with a
+//    full/empty mbarrier pair (double-buffered in the down GEMM).
+//  * Operands are K-major bf16 tiles of 64 elements (128 B) per row, loaded by
+//    TMA with the 128-byte swizzle that the tcgen05 shared-memory descriptor
+//    expects; the token tile is loaded in 32-row boxes, only as many as the
+//    segment needs.  Rows past a segment belong to the next expert (or are
+//    zero-filled past the matrix); their results are computed and dropped.
+//  * Tiles are enumerated expert-major, feature-tile next, token-tile last, so
+//    CTAs that run at the same time share weight tiles and token tiles in L2.
+//  * Every mbarrier wait is bounded (about 1 s); on expiry the kernel sets the
+//    error word, waits briefly for its own copies and MMAs in flight, frees
+//    tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int BM = 128;         // features per tile (MMA M)
+constexpr int BK = 64;          // K per stage: one 128-byte swizzle atom row
+constexpr int BN_MAX = 256;     // tokens per tile (MMA N upper bound)
+constexpr int B_BOX = 32;       // token rows per TMA box
+constexpr int A_TILE_BYTES = BM * BK * 2;      // 16 KB
+constexpr int B_TILE_BYTES = BN_MAX * BK * 2;  // 32 KB
+constexpr int B_BOX_BYTES = B_BOX * BK * 2;    // 4 KB
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr int MAX_E = 1024;
+
+template <int MODE>
+struct Cfg;
+template <>
+struct Cfg<0> {  // gate/up + SwiGLU: two A tiles (W1, W3) per stage
+    static constexpr int NUM_A = 2, STAGES = 3, ACC_STAGES = 1;
+};
+template <>
+struct Cfg<1> {  // down: one A tile per stage, double-buffered accumulator
+    static constexpr int NUM_A = 1, STAGES = 4, ACC_STAGES = 2;
+};
+
+template <int MODE>
+__host__ __device__ constexpr int stage_bytes() { return Cfg<MODE>::NUM_A * A_TILE_BYTES + B_TILE_BYTES; }
+
+template <int MODE>
+__host__ __device__ constexpr size_t smem_bytes() {
+    // 1 KB alignment slack + stages + barriers/tmem slot + schedule table
+    return 1024 + (size_t)Cfg<MODE>::STAGES * stage_bytes<MODE>() + 256 + sizeof(int) * (MAX_E + 2);
+}
+
+struct Params {
+    const int32_t* offsets;  // [E+1], or NULL: one segment [0, rows)
+    int E;
+    int rows;                // rows of the activation matrix
+    int K;                   // reduction length
+    int N_out;               // output features per expert
+    int a_rows;              // weight rows per expert in the 2D weight view
+    int up_off;              // row offset of W3 inside an expert (gate/up only)
+    void* out;               // H bf16 [rows, N_out] or Y fp32 [rows, N_out]
+    uint32_t* err;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity.  Returns false if the
+// kernel is aborting (flag set by any role) or if this wait ran out.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       uint32_t* err, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = moe::globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (moe::globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            moe::raise_error(err, moe::ERR_TIMEOUT_PIPE);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row
+// core-matrix groups 1024 bytes apart (stride byte offset), version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);  // start address
+    d |= (uint64_t)1 << 16;                   // leading byte offset (unused for SW128 K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset
+    d |= (uint64_t)1 << 46;                   // descriptor version
+    d |= (uint64_t)2 << 61;                   // swizzle: 128 B
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M=128.
+__device__ __forceinline__ uint32_t idesc_bf16(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- schedule
+
+struct Unit {
+    int e;        // expert
+    int m_start;  // first activation row of the token tile
+    int n_tok;    // tokens in the tile (1..256)
+    int n0;       // first output feature
+};
+
+// Units of expert e occupy [mpre[e] * nt, mpre[e+1] * nt); inside, the feature
+// tile is the major index and the token tile the minor one.
+__device__ __forceinline__ Unit decode_unit(int u, const int* mpre, const int* offs, int E,
+                                            int n_tiles) {
+    int lo = 0, hi = E;  // find e with mpre[e]*nt <= u < mpre[e+1]*nt
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (mpre[mid] * n_tiles <= u) lo = mid; else hi = mid;
+    }
+    const int e = lo;
+    const int mt = mpre[e + 1] - mpre[e];
+    const int local = u - mpre[e] * n_tiles;
+    const int nt = local / mt, mtile = local - nt * mt;
+    Unit r;
+    r.e = e;
+    r.m_start = offs[e] + mtile * BN_MAX;
+    r.n_tok = min(BN_MAX, offs[e + 1] - r.m_start);
+    r.n0 = nt * BM;
+    return r;
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a,
+                           const __grid_constant__ CUtensorMap tm_b, const Params p) {
+    using C = Cfg<MODE>;
+    constexpr int STAGES = C::STAGES, NUM_A = C::NUM_A, ACC = C::ACC_STAGES;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte aligned base for the swizzled tiles
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* tiles = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)STAGES * stage_bytes<MODE>());
+    uint64_t* full_bar = bars;                  // [STAGES]
+    uint64_t* empty_bar = bars + STAGES;        // [STAGES]
+    uint64_t* tfull_bar = bars + 2 * STAGES;    // [ACC]
+    uint64_t* tempty_bar = tfull_bar + ACC;     // [ACC]
+    uint64_t* drain_bar = tempty_bar + ACC;     // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* total_units = reinterpret_cast<int*>(tmem_slot + 2);
+    int* mpre = reinterpret_cast<int*>(smem + (size_t)STAGES * stage_bytes<MODE>() + 256);
+    // offsets are re-read from global (read-only, L1/L2 resident)
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ---- schedule: token tiles per expert and their prefix (warp 0) -------
+    const int E = p.E;
+    const int n_tiles = (p.N_out + BM - 1) / BM;
+    if (warp == 0) {
+        // per-lane chunk of experts, then a warp scan of the chunk sums
+        const int per = (E + 31) / 32;
+        const int lo = min(E, lane * per), hi = min(E, lo + per);
+        int sum = 0;
+        bool bad = false;
+        for (int e = lo; e < hi; ++e) {
+            const int a = p.offsets ? p.offsets[e] : 0;
+            const int b = p.offsets ? p.offsets[e + 1] : p.rows;
+            if (a < 0 || b < a || b > p.rows) bad = true;
+            sum += (b - a + BN_MAX - 1) / BN_MAX;
+        }
+        int inc = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off) inc += o;
+        }
+        int run = inc - sum;
+        for (int e = lo; e < hi; ++e) {
+            mpre[e] = run;
+            const int a = p.offsets ? p.offsets[e] : 0;
+            const int b = p.offsets ? p.offsets[e + 1] : p.rows;
+            run += (b - a + BN_MAX - 1) / BN_MAX;
+        }
+        const bool any_bad = __any_sync(0xffffffffu, bad);
+        if (lane == 31) {
+            mpre[E] = inc;
+            // an earlier stage that failed, or inconsistent offsets: no work
+            *total_units = (any_bad || moe::read_error(p.err)) ? -1 : inc * n_tiles;
+            if (any_bad) moe::raise_error(p.err, moe::ERR_BAD_OFFSETS);
+        }
+    }
+    if (tid == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int a = 0; a < ACC; ++a) {
+            mbar_init(smem_u32(&tfull_bar[a]), 1);
+            mbar_init(smem_u32(&tempty_bar[a]), 4);
+        }
+        mbar_init(smem_u32(drain_bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int U = *total_units;
+
+    // offsets for decode: dense mode synthesises {0, rows}
+    __shared__ int s_dense_offs[2];
+    if (tid == 0) {
+        s_dense_offs[0] = 0;
+        s_dense_offs[1] = p.rows;
+    }
+    __syncthreads();
+    const int* offs = p.offsets ? p.offsets : s_dense_offs;
+    const int num_kb = (p.K + BK - 1) / BK;
+
+    if (U > 0 && warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long issued = 0;
+            for (int u = blockIdx.x; u < U && !*abort_flag; u += gridDim.x) {
+                const Unit t = decode_unit(u, mpre, offs, E, n_tiles);
+                const int nbox = (t.n_tok + B_BOX - 1) / B_BOX;
+                const uint32_t bytes = NUM_A * A_TILE_BYTES + nbox * B_BOX_BYTES;
+                const int a_row = t.e * p.a_rows + t.n0;
+                bool ok = true;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, p.err,
+                                   moe::WAIT_LIMIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = tiles + (size_t)stage * stage_bytes<MODE>();
+                    const uint32_t fb = smem_u32(&full_bar[stage]);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    const int kx = kb * BK;
+                    tma_load_2d(smem_u32(st), &tm_a, fb, kx, a_row);
+                    if (NUM_A == 2) tma_load_2d(smem_u32(st + A_TILE_BYTES), &tm_a, fb, kx, a_row + p.up_off);
+                    uint8_t* bdst = st + NUM_A * A_TILE_BYTES;
+                    for (int j = 0; j < nbox; ++j)
+                        tma_load_2d(smem_u32(bdst + j * B_BOX_BYTES), &tm_b, fb, kx,
+                                    t.m_start + j * B_BOX);
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+            }
+            if (*abort_flag) {
+                // let the copies this thread started land before the CTA exits
+                for (int i = 0; i < STAGES && issued > 0; ++i, --issued) {
+                    if (stage == 0) { stage = STAGES; phase ^= 1; }
+                    --stage;
+                    const uint64_t t0 = moe::globaltimer_ns();
+                    while (!mbar_try_wait(smem_u32(&full_bar[stage]), phase) &&
+                           moe::globaltimer_ns() - t0 < 10000000ull) {
+                    }
+                }
+            }
+        }
+    } else if (U > 0 && warp == 1) {
+        // ================= MMA issuer (one thread) =================
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool issued_any = false;
+            for (int u = blockIdx.x; u < U && !*abort_flag; u += gridDim.x) {
+                const Unit t = decode_unit(u, mpre, offs, E, n_tiles);
+                const int bn = (t.n_tok + 15) & ~15;
+                const uint32_t idesc = idesc_bf16(bn);
+                if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, abort_flag, p.err,
+                               moe::WAIT_LIMIT_NS))
+                    break;
+                tc_fence_after();
+                const uint32_t d0 = tmem_base + (uint32_t)(acc * 256);
+                bool ok = true;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&full_bar[stage]), phase, abort_flag, p.err,
+                                   moe::WAIT_LIMIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = smem_u32(tiles + (size_t)stage * stage_bytes<MODE>());
+                    const uint32_t bsm = st + NUM_A * A_TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t bdesc = smem_desc_sw128(bsm + kk * 32);
+                        const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+                        mma_bf16(d0, smem_desc_sw128(st + kk * 32), bdesc, idesc, accum);
+                        if (NUM_A == 2)
+                            mma_bf16(d0 + 256, smem_desc_sw128(st + A_TILE_BYTES + kk * 32), bdesc,
+                                     idesc, accum);
+                    }
+                    issued_any = true;
+                    mma_commit(smem_u32(&empty_bar[stage]));  // frees the stage when done
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&tfull_bar[acc]));  // accumulator ready
+                if (++acc == ACC) { acc = 0; acc_phase ^= 1; }
+            }
+            if (issued_any) {
+                // wait until every MMA of this thread has completed
+                mma_commit(smem_u32(drain_bar));
+                const uint64_t t0 = moe::globaltimer_ns();
+                while (!mbar_try_wait(smem_u32(drain_bar), 0) &&
+                       moe::globaltimer_ns() - t0 < moe::WAIT_LIMIT_NS) {
+                }
+            }
+        }
+    } else if (U > 0 && warp >= 2) {
+        // ================= epilogue: tensor memory -> global =================
+        const int q = warp & 3;  // this warp's quarter of the 128 TMEM lanes
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < U; u += gridDim.x) {
+            const Unit t = decode_unit(u, mpre, offs, E, n_tiles);
+            if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.err,
+                           moe::WAIT_LIMIT_NS))
+                break;
+            tc_fence_after();
+            const int n = t.n0 + q * 32 + lane;
+            const bool n_ok = n < p.N_out;
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 256);
+            for (int c0 = 0; c0 < t.n_tok; c0 += 32) {
+                uint32_t g[32];
+                tmem_ld32(tbase + c0, g);
+                if (MODE == 0) {
+                    uint32_t up[32];
+                    tmem_ld32(tbase + 256 + c0, up);
+                    tmem_wait_ld();
+                    __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int tok = c0 + j;
+                        if (n_ok && tok < t.n_tok) {
+                            const float gv = __uint_as_float(g[j]);
+                            const float uv = __uint_as_float(up[j]);
+                            const float h = gv / (1.0f + __expf(-gv)) * uv;
+                            H[(size_t)(t.m_start + tok) * p.N_out + n] = __float2bfloat16_rn(h);
+                        }
+                    }
+                } else {
+                    tmem_wait_ld();
+                    float* Y = static_cast<float*>(p.out);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int tok = c0 + j;
+                        if (n_ok && tok < t.n_tok)
+                            Y[(size_t)(t.m_start + tok) * p.N_out + n] = __uint_as_float(g[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
+            if (++acc == ACC) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// 2D bf16 tensor map over a row-major [rows, cols] matrix, box {64, box_rows},
+// 128-byte swizzle, zero fill outside.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int MODE>
+int launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t s) {
+    static bool attr_done = false;
+    const size_t smem = smem_bytes<MODE>();
+    if (!attr_done) {
+        if (cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr_done = true;
+    }
+    grouped_gemm_tc_kernel<MODE><<<moe_host::num_sms(), NUM_THREADS, smem, s>>>(a, b, p);
+    return moe_host::launch_status();
+}
+
+}  // namespace
+
+namespace moe_tc {
+
+// Both GEMMs of the SwiGLU FFN over bf16 rows; offsets == NULL means one
+// segment [0, rows) with expert 0 (dense, e.g. the shared expert).
+int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
+                     const void* w13, const void* w2, float* y, void* h, uint32_t* err,
+                     cudaStream_t s, cudaEvent_t between) {
+    if (E > MAX_E) return MOE_ERR_UNSUPPORTED;
+    CUtensorMap a1, b1, a2, b2;
+    if (!make_map(&a1, w13, (uint64_t)E * 2 * I, d, BM) ||
+        !make_map(&b1, x_perm, rows, d, B_BOX) ||
+        !make_map(&a2, w2, (uint64_t)E * d, I, BM) ||
+        !make_map(&b2, h, rows, I, B_BOX))
+        return MOE_ERR_CUDA;
+    Params p1{offsets, E, rows, d, I, 2 * I, I, h, err};
+    int rc = launch<0>(a1, b1, p1, s);
+    if (rc != MOE_OK) return rc;
+    if (between && cudaEventRecord(between, s) != cudaSuccess) return MOE_ERR_CUDA;
+    Params p2{offsets, E, rows, I, d, d, 0, y, err};
+    return launch<1>(a2, b2, p2, s);
+}
+
+}  // namespace moe_tc

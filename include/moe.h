@@ -1,0 +1,204 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) Mixture-of-Experts layer hot path.
+ *
+ * One MoE layer on one GPU: router scoring and top-k selection, dispatch
+ * (per-expert histogram, scan, permute), the per-expert SwiGLU FFN as grouped
+ * GEMMs, and the gate-weighted combine.  The layer is the DeepSeek-V3 MoE layer
+ * that "CUCo: An Agentic Framework for Compute and Communication Co-design"
+ * uses as a headline workload (abstract; Table 4, row "MoE Dispatch/Combine":
+ * dispatch and combine around local expert compute).  The pages do not write
+ * the arithmetic down; each entry point states the reading it implements.
+ *
+ * Conventions for every entry point
+ *   - Every array argument is a DEVICE pointer unless stated otherwise; the
+ *     caller allocates and owns all of them.  The library never allocates,
+ *     frees or keeps memory between calls and holds no global state.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; nothing synchronises.
+ *   - Return value: a moe_status.  Invalid arguments are detected on the host
+ *     before anything is enqueued (MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *     MOE_ERR_WORKSPACE).  MOE_ERR_CUDA means a launch failed.
+ *   - Kernels never spin without bound.  A wait that runs out (about one
+ *     second) or an inconsistent device-side input (e.g. non-monotone
+ *     offsets) makes the kernel stop early and set the workspace's error word;
+ *     moe_check_error() reports it.  Outputs of such a call are unspecified.
+ *   - Row-major layouts throughout; T tokens, d hidden size, E routed experts,
+ *     k experts per token, I expert intermediate size, S = T*k slots.
+ *   - Pointers to bf16 / fp32 / int32 arrays must be 16-byte aligned; d and I
+ *     must be multiples of 8 (16-byte rows for the bulk-copy engine).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or config   */
+    MOE_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels handle     */
+    MOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required    */
+    MOE_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed          */
+    MOE_ERR_TIMEOUT = 5,      /* a bounded device wait ran out (error word)    */
+    MOE_ERR_DEVICE_INPUT = 6  /* a kernel found inconsistent device-side input */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef enum {
+    MOE_SCORE_SOFTMAX = 0,  /* scores are the router logits; gates from softmax */
+    MOE_SCORE_SIGMOID = 1   /* scores are sigmoid(logits); gates from scores     */
+} moe_score_fn;
+
+/* Routing configuration.
+ *   num_experts  E (1..1024)
+ *   top_k        k (1..32, k <= eligible experts)
+ *   n_group      number of contiguous expert groups (1 = no group limit);
+ *                E % n_group == 0, group size >= 2 when n_group > 1, n_group <= 32
+ *   topk_group   groups kept per token (1..n_group)
+ *   score_fn     moe_score_fn
+ *   routed_scale gates are multiplied by this after normalisation (1.0, 2.5) */
+typedef struct {
+    int32_t num_experts;
+    int32_t top_k;
+    int32_t n_group;
+    int32_t topk_group;
+    int32_t score_fn;
+    float routed_scale;
+} moe_route_cfg;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* moe_status_string(int status);
+
+/* ABI version (major * 100 + minor). */
+int moe_version(void);
+
+/* ---------------------------------------------------------------- routing */
+
+/* Top-k selection and gates from a given fp32 score tensor.
+ *   scores   [T,E] fp32: logits (softmax) or sigmoid outputs (sigmoid)
+ *   bias     [E] fp32 or NULL: added to the scores for SELECTION only
+ *            (DeepSeek-V3 style); must be NULL for softmax
+ *   topk_idx [T,k] int32 out: experts in selection order -- descending key
+ *            (score + bias), equal keys by ascending expert index
+ *   topk_w   [T,k] fp32 out: softmax: p_j / sum_sel p with p = softmax over
+ *            all E; sigmoid: s_j / sum_sel s; both times routed_scale
+ * With n_group > 1, each group's score is the sum of its two largest keys and
+ * only the topk_group best groups (ties to the lower group) stay eligible.
+ * Selection compares fp32 keys exactly; ties go to the lower index. */
+int moe_route_from_scores(const float* scores, const float* bias, int T,
+                          const moe_route_cfg* cfg, int32_t* topk_idx, float* topk_w,
+                          void* stream);
+
+/* Router GEMM then moe_route_from_scores.
+ *   x        [T,d] bf16 or fp32 (dtype)
+ *   w_router [E,d] fp32
+ *   scores   [T,E] fp32 out (logits, or sigmoid(logits)); fp32 accumulate */
+int moe_route(const void* x, int dtype, const float* w_router, const float* bias, int T, int d,
+              const moe_route_cfg* cfg, float* scores, int32_t* topk_idx, float* topk_w,
+              void* stream);
+
+/* --------------------------------------------------------------- dispatch */
+
+/* Workspace bytes moe_dispatch needs for T tokens, k slots, E experts. */
+size_t moe_dispatch_workspace_size(int T, int k, int E);
+
+/* Stable counting sort of the S = T*k slots (s = t*k + j) by expert, then the
+ * row gather.  Outputs (all int32 unless noted):
+ *   counts[E]        slots routed to each expert
+ *   offsets[E+1]     exclusive prefix of counts, offsets[E] = S
+ *   slot_to_row[S]   row(s) = offsets[e] + #{s' < s : idx(s') = e}
+ *   row_to_token[S]  t such that row lies in token t's slots
+ *   x_perm [S,d]     x_perm[row(s)] = x[s / k]  (dtype of x; may be NULL to
+ *                    compute the index maps only)
+ * topk_idx entries must lie in [0,E); others set the error word and leave
+ * the outputs unspecified.  ws: moe_dispatch_workspace_size bytes, any
+ * contents; its first 16 bytes hold the error word (see moe_check_error). */
+int moe_dispatch(const int32_t* topk_idx, const void* x, int dtype, int T, int d, int k, int E,
+                 int32_t* counts, int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_token,
+                 void* x_perm, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------ expert FFN */
+
+/* Workspace bytes moe_grouped_ffn needs for `rows` permuted rows. */
+size_t moe_grouped_ffn_workspace_size(int rows, int d, int I, int dtype);
+
+/* Per-expert SwiGLU FFN over permuted rows, as two grouped GEMMs:
+ *   rows [offsets[e], offsets[e+1]) belong to expert e (offsets on device,
+ *   E+1 int32, non-decreasing, offsets[E] <= rows);
+ *   H[r]  = silu(x_perm[r] W1_e^T) * (x_perm[r] W3_e^T)   (bf16 for bf16)
+ *   y[r]  = H[r] W2_e^T                                     (fp32)
+ *   w13 [E,2I,d]: rows 0..I-1 are W1 (gate), rows I..2I-1 are W3 (up)
+ *   w2  [E,d,I]
+ *   x_perm [rows,d], y_perm [rows,d] fp32 (rows past offsets[E] untouched).
+ * bf16 runs on the tcgen05 tensor cores with fp32 accumulation; fp32 runs on
+ * the CUDA cores in fp32.  Experts with no rows read none of their weights.
+ * ws: moe_grouped_ffn_workspace_size bytes (holds H and the error word). */
+int moe_grouped_ffn(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
+                    const void* w13, const void* w2, int dtype, float* y_perm, void* ws,
+                    size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- combine */
+
+/* out[t,:] = sum_{j<k} topk_w[t,j] * y_perm[slot_to_row[t*k+j], :]  (+ shared[t,:])
+ * summed in slot order in fp32.  y_perm [S,d] fp32, shared [T,d] fp32 or NULL,
+ * out [T,d] fp32 (must not alias the inputs). */
+int moe_combine(const float* y_perm, const int32_t* slot_to_row, const float* topk_w,
+                const float* shared, int T, int k, int d, float* out, void* stream);
+
+/* ---------------------------------------------------------- the whole layer */
+
+/* Number of stage-boundary events moe_layer records when asked (see below). */
+#define MOE_LAYER_EVENTS 7
+
+/* Inputs of one MoE layer.  Expert weights and x share `dtype`; the router
+ * weight and bias are fp32.  w13_sh/w2_sh (shared expert, [2I_sh,d] and
+ * [d,I_sh], gate weight 1) may be NULL with I_sh = 0.  The optional outputs,
+ * when non-NULL, receive the intermediate routing results.
+ * stage_events, when non-NULL, points to MOE_LAYER_EVENTS cudaEvent_t handles
+ * (host array, caller-created) that moe_layer records on `stream` at: start,
+ * after the router GEMM, after top-k, after dispatch, after the routed gate/up
+ * GEMM, after the routed down GEMM, and at the end (after combine).  They
+ * let a caller time each stage inside a run of the whole layer. */
+typedef struct {
+    const void* x;          /* [T,d]   */
+    const float* w_router;  /* [E,d]   */
+    const float* bias;      /* [E] or NULL */
+    const void* w13;        /* [E,2I,d] */
+    const void* w2;         /* [E,d,I]  */
+    const void* w13_sh;     /* [2I_sh,d] or NULL */
+    const void* w2_sh;      /* [d,I_sh]  or NULL */
+    int32_t T, d, I, I_sh, dtype;
+    moe_route_cfg route;
+    float* scores_out;      /* [T,E]  or NULL */
+    int32_t* topk_idx_out;  /* [T,k]  or NULL */
+    float* topk_w_out;      /* [T,k]  or NULL */
+    int32_t* offsets_out;   /* [E+1]  or NULL */
+    void* const* stage_events; /* MOE_LAYER_EVENTS cudaEvent_t, or NULL */
+} moe_layer_args;
+
+/* Workspace bytes moe_layer needs. */
+size_t moe_layer_workspace_size(const moe_layer_args* a);
+
+/* out [T,d] fp32 = the layer: route, dispatch, grouped FFN, shared expert,
+ * combine.  `stream2` (may be NULL) is a second stream of the same device:
+ * when given, the shared expert runs on it concurrently with the routed path,
+ * ordered by events; everything is complete on `stream` when the call's work
+ * finishes there. */
+int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, void* stream,
+              void* stream2);
+
+/* Synchronises `stream`, reads and clears the error word of `ws` (a workspace
+ * previously passed to moe_dispatch / moe_grouped_ffn / moe_layer).  Returns
+ * MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_INPUT or MOE_ERR_CUDA.  `detail`
+ * (host pointer, may be NULL) receives the raw error word. */
+int moe_check_error(void* ws, void* stream, uint32_t* detail);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

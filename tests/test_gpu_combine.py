@@ -1,0 +1,49 @@
+"""Gate-weighted combine on the GPU (moe_combine) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from combine_router_gemm_gb300 import binding as B
+from helpers import cuda_f32, np_
+
+pytestmark = pytest.mark.gpu
+
+
+def perm_maps(T, k, seed):
+    g = torch.Generator()
+    g.manual_seed(seed)
+    s2r = torch.randperm(T * k, generator=g).to(torch.int32)
+    return s2r
+
+
+@pytest.mark.parametrize("T,k,d,shared", [(4096, 8, 7168, True), (300, 2, 4096, False),
+                                          (1, 1, 8, True), (77, 5, 40, False)])
+def test_combine(oracle, T, k, d, shared):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(T + d)
+    y = torch.randn((T * k, d), generator=g, device="cuda")
+    w = torch.rand((T, k), generator=g, device="cuda")
+    sh = torch.randn((T, d), generator=g, device="cuda") if shared else None
+    s2r = perm_maps(T, k, T).cuda()
+    out = cuda_f32((T, d))
+    B.moe_combine(y, s2r, w, sh, out)
+    torch.cuda.synchronize()
+    ref = oracle.combine(np_(y), np_(s2r), np_(w), np_(sh), T, k)
+    np.testing.assert_allclose(np_(out), ref, rtol=2e-6, atol=2e-6)
+
+
+def test_combine_identity_experts(oracle):
+    # y rows are the tokens' own rows: out[t] = (sum_j w[t,j]) * x[t].
+    T, k, d = 500, 4, 256
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1)
+    x = torch.randn((T, d), generator=g, device="cuda")
+    s2r = perm_maps(T, k, 2).cuda()
+    r2t = torch.empty(T * k, dtype=torch.long, device="cuda")
+    r2t[s2r.long()] = torch.arange(T * k, device="cuda") // k
+    y = x[r2t].contiguous()
+    w = torch.rand((T, k), generator=g, device="cuda")
+    out = cuda_f32((T, d))
+    B.moe_combine(y, s2r, w, None, out)
+    ref = w.double().sum(1, keepdim=True) * x.double()
+    np.testing.assert_allclose(np_(out), np_(ref), rtol=1e-6, atol=1e-6)

@@ -1,0 +1,109 @@
+"""Grouped SwiGLU FFN on the GPU (moe_grouped_ffn) against the oracle.
+
+bf16 runs on the tcgen05 tensor cores: compared with the oracle's double
+result (h rounded to bf16 once) at the bf16 layer tolerances.  fp32 runs on
+the CUDA cores: relative Frobenius 1e-5.  Segments are ragged, span several
+256-token tiles, include empty experts, and feature/K sizes include tails.
+"""
+import numpy as np
+import pytest
+import torch
+
+from combine_router_gemm_gb300 import binding as B
+from helpers import F32_REL_FRO, assert_bf16_close, cuda_f32, np_, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+
+def make_case(E, d, I, counts, dtype, seed, wstd=0.06, extra_rows=0):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    counts = torch.tensor(counts, dtype=torch.int64)
+    offsets = torch.zeros(E + 1, dtype=torch.int32)
+    offsets[1:] = torch.cumsum(counts, 0).to(torch.int32)
+    rows = int(offsets[-1]) + extra_rows
+    x = torch.randn((rows, d), generator=g, device="cuda").to(dtype)
+    w13 = (torch.randn((E, 2 * I, d), generator=g, device="cuda") * wstd).to(dtype)
+    w2 = (torch.randn((E, d, I), generator=g, device="cuda") * wstd).to(dtype)
+    return x, offsets.cuda(), w13, w2
+
+
+def run_ffn(x, offsets, w13, w2):
+    rows, d = x.shape
+    I = w2.shape[2]
+    dt = B.BF16 if x.dtype == torch.bfloat16 else B.F32
+    y = torch.full((rows, d), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(B.moe_grouped_ffn_workspace_size(rows, d, I, dt), dtype=torch.uint8,
+                     device="cuda")
+    B.moe_grouped_ffn(x, offsets, w13, w2, y, ws)
+    rc, detail = B.moe_check_error(ws)
+    assert rc == B.OK, detail
+    return y
+
+
+CASES = [
+    # E, d, I, counts
+    (4, 128, 128, [1, 0, 300, 17]),                 # 300 rows: two token tiles
+    (8, 256, 256, [5, 40, 0, 0, 256, 257, 3, 100]),  # exact tile boundary 256 / 257
+    (3, 192, 136, [33, 64, 511]),                    # I tail (136 = 128 + 8), d = 3 K-blocks
+    (2, 200, 264, [16, 15]),                         # K tail (200 = 3*64 + 8), N tail
+    (1, 512, 384, [1000]),                           # dense, many tiles
+    (16, 64, 128, [0] * 7 + [9] + [0] * 8),          # one active expert of 16
+]
+
+
+@pytest.mark.parametrize("E,d,I,counts", CASES)
+def test_grouped_ffn_bf16(oracle, E, d, I, counts):
+    x, offsets, w13, w2 = make_case(E, d, I, counts, torch.bfloat16, seed=E * 1000 + d)
+    y = run_ffn(x, offsets, w13, w2)
+    torch.cuda.synchronize()
+    n = int(offsets[-1])
+    ref = oracle.grouped_ffn(np_(x), np_(offsets), np_(w13), np_(w2), round_h=True)
+    assert_bf16_close(np_(y)[:n], ref, f"E={E} d={d} I={I}")
+    assert rel_fro(np_(y)[:n], ref) < 2e-3
+
+
+def test_grouped_ffn_rows_past_offsets_untouched(oracle):
+    x, offsets, w13, w2 = make_case(3, 128, 128, [10, 0, 20], torch.bfloat16, seed=3,
+                                    extra_rows=50)
+    y = run_ffn(x, offsets, w13, w2)
+    assert torch.isnan(y[30:]).all()
+
+
+def test_grouped_ffn_empty_experts_never_read(oracle):
+    # NaN weights on experts without rows must not reach the output.
+    E, d, I = 6, 128, 128
+    counts = [40, 0, 70, 0, 0, 5]
+    x, offsets, w13, w2 = make_case(E, d, I, counts, torch.bfloat16, seed=11)
+    w13n, w2n = w13.clone(), w2.clone()
+    for e in (1, 3, 4):
+        w13n[e] = float("nan")
+        w2n[e] = float("nan")
+    y = run_ffn(x, offsets, w13n, w2n)
+    y0 = run_ffn(x, offsets, w13, w2)
+    assert torch.isfinite(y[:115]).all()
+    assert torch.equal(y[:115], y0[:115])
+
+
+@pytest.mark.parametrize("E,d,I,counts", [(8, 128, 256, [20, 0, 7, 33, 1, 0, 50, 17]),
+                                           (2, 40, 24, [3, 9])])
+def test_grouped_ffn_f32(oracle, E, d, I, counts):
+    x, offsets, w13, w2 = make_case(E, d, I, counts, torch.float32, seed=7, wstd=0.1)
+    y = run_ffn(x, offsets, w13, w2)
+    n = int(offsets[-1])
+    ref = oracle.grouped_ffn(np_(x), np_(offsets), np_(w13), np_(w2), round_h=False)
+    assert rel_fro(np_(y)[:n], ref) <= F32_REL_FRO
+
+
+def test_grouped_ffn_bad_offsets_flagged():
+    # Non-monotone device offsets: the kernels do no work and flag the input.
+    x, offsets, w13, w2 = make_case(2, 128, 128, [10, 10], torch.bfloat16, seed=1)
+    offsets[1] = 15
+    offsets[2] = 12
+    rows, d = x.shape
+    y = cuda_f32((rows, d))
+    ws = torch.empty(B.moe_grouped_ffn_workspace_size(rows, d, 128, B.BF16), dtype=torch.uint8,
+                     device="cuda")
+    B.moe_grouped_ffn(x, offsets, w13, w2, y, ws)
+    rc, detail = B.moe_check_error(ws)
+    assert rc == B.ERR_DEVICE_INPUT and detail != 0

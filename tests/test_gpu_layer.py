@@ -1,0 +1,115 @@
+"""The whole layer (moe_layer) against the oracle.
+
+Small workloads are checked on every token; the full-size workloads are run
+exactly as the benchmark runs them (same entry point, second stream for the
+shared expert) and checked on a seeded sample of tokens, which the oracle can
+evaluate one by one, plus properties that hold at any size.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+from combine_router_gemm_gb300 import binding as B
+from combine_router_gemm_gb300 import inputs
+from helpers import F32_REL_FRO, assert_bf16_close, cuda_f32, cuda_i32, near_tie_tokens, np_, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+
+def run_layer(cfg, inp, overlap=True):
+    T = cfg.T
+    layer = B.MoELayer(inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"],
+                       inp["w2_sh"], B.cfg_from(cfg), T, overlap=overlap)
+    idx, w = cuda_i32((T, cfg.k)), cuda_f32((T, cfg.k))
+    scores, offs = cuda_f32((T, cfg.E)), cuda_i32(cfg.E + 1)
+    out = layer.forward(inp["x"], scores_out=scores, topk_idx_out=idx, topk_w_out=w,
+                        offsets_out=offs)
+    rc, detail = B.moe_check_error(layer.ws)
+    assert rc == B.OK, detail
+    return out, idx, w, scores, offs
+
+
+def oracle_tokens(oracle, cfg, inp, tok, needed_experts=None):
+    """Oracle on the tokens `tok`; expert weights copied to the host only for
+    the experts the oracle itself selects for them."""
+    fn = oracle.SIGMOID if cfg.score_fn == "sigmoid" else oracle.SOFTMAX
+    x = np_(inp["x"][tok])
+    wr = np_(inp["w_router"])
+    bias = np_(inp["bias"])
+    sc = oracle.router_scores(x, wr, fn)
+    sel = oracle.select(sc, cfg.k, bias=bias if fn == oracle.SIGMOID else None,
+                        n_group=cfg.n_group, topk_group=cfg.topk_group)
+    experts = np.unique(sel)
+    w13 = np.empty(tuple(inp["w13"].shape), np.uint16 if cfg.dtype == "bf16" else np.float32)
+    w2 = np.empty(tuple(inp["w2"].shape), w13.dtype)
+    for e in experts:
+        w13[e] = np_(inp["w13"][int(e)])
+        w2[e] = np_(inp["w2"][int(e)])
+    idx, w, out = oracle.moe_tokens(
+        x, E=cfg.E, k=cfg.k, w13=w13, w2=w2, w_router=wr, bias=bias, n_group=cfg.n_group,
+        topk_group=cfg.topk_group, score_fn=fn, routed_scale=cfg.routed_scale,
+        w13_sh=np_(inp["w13_sh"]), w2_sh=np_(inp["w2_sh"]), round_h=cfg.dtype == "bf16")
+    return sc, idx, w, out
+
+
+def test_layer_tiny_fp32_all_tokens(oracle):
+    cfg = inputs.CONFIGS["tiny_fp32"]
+    inp = inputs.make_inputs(cfg, seed=0, device="cuda")
+    out, idx, w, scores, offs = run_layer(cfg, inp)
+    sc, ridx, rw, rout = oracle_tokens(oracle, cfg, inp, torch.arange(cfg.T, device="cuda"))
+    np.testing.assert_array_equal(np_(idx), ridx)
+    np.testing.assert_allclose(np_(w), rw, rtol=1e-5)
+    assert rel_fro(np_(out), rout) <= F32_REL_FRO
+
+
+SMALL_BF16 = [
+    inputs.MoEConfig("small_dsv3", T=700, d=256, E=32, k=4, I=128, dtype="bf16",
+                     score_fn="sigmoid", n_group=4, topk_group=2, routed_scale=2.5,
+                     shared_I=128, bias="normal", expert_std=0.06, router_std=0.06),
+    inputs.MoEConfig("small_mixtral", T=513, d=384, E=8, k=2, I=256, dtype="bf16",
+                     expert_std=0.05),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL_BF16, ids=lambda c: c.name)
+@pytest.mark.parametrize("overlap", [True, False])
+def test_layer_small_bf16_all_tokens(oracle, cfg, overlap):
+    inp = inputs.make_inputs(cfg, seed=1, device="cuda")
+    out, idx, w, scores, offs = run_layer(cfg, inp, overlap)
+    sc, ridx, rw, rout = oracle_tokens(oracle, cfg, inp, torch.arange(cfg.T, device="cuda"))
+    same = (np_(idx) == ridx).all(1)
+    amb = near_tie_tokens(sc, np_(inp["bias"]), cfg.k, cfg.n_group, cfg.topk_group)
+    assert (same | amb).all()
+    assert_bf16_close(np_(out)[same], rout[same], cfg.name)
+
+
+FULL = ["mixtral_bf16", "dsv3_prefill", "dsv3_decode", "dsv3_zipf"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_layer_full_size_sampled(oracle, name):
+    cfg = inputs.CONFIGS[name]
+    inp = inputs.make_inputs(cfg, seed=0, device="cuda")
+    out, idx, w, scores, offs = run_layer(cfg, inp, overlap=True)
+    torch.cuda.synchronize()
+    # properties at full size
+    assert torch.isfinite(out).all()
+    o = np_(offs)
+    assert o[0] == 0 and o[-1] == cfg.S and (np.diff(o) >= 0).all()
+    if cfg.bias == "zipf":
+        assert (np.diff(o) == 0).sum() >= cfg.zipf_zero
+    # sampled tokens against the oracle
+    g = torch.Generator()
+    g.manual_seed(7)
+    tok = torch.randperm(cfg.T, generator=g)[: min(24, cfg.T)].sort().values
+    sc, ridx, rw, rout = oracle_tokens(oracle, cfg, inp, tok.cuda())
+    gidx = np_(idx[tok.cuda()])
+    same = (gidx == ridx).all(1)
+    amb = near_tie_tokens(sc, np_(inp["bias"]), cfg.k, cfg.n_group, cfg.topk_group)
+    assert (same | amb).all()
+    assert_bf16_close(np_(out[tok.cuda()])[same], rout[same], name)
+    del inp, out
+    gc.collect()
+    torch.cuda.empty_cache()

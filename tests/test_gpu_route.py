@@ -1,0 +1,73 @@
+"""Routing on the GPU (moe_route_from_scores, moe_route) against the oracle.
+
+Given the same fp32 score tensor, chosen experts must match bit for bit
+(including order and tie-breaking) and gates within GATE_RTOL.
+"""
+import numpy as np
+import pytest
+import torch
+
+from combine_router_gemm_gb300 import binding as B
+from combine_router_gemm_gb300 import inputs
+from helpers import GATE_RTOL, cuda_f32, cuda_i32, near_tie_tokens, np_
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # T, E, k, n_group, topk_group, score_fn, bias, quant_bits, scale
+    (4096, 8, 2, 1, 1, "softmax", False, None, 1.0),      # Mixtral routing
+    (4096, 8, 2, 1, 1, "softmax", False, 2, 1.0),         # heavy ties
+    (4096, 256, 8, 8, 4, "sigmoid", True, None, 2.5),     # DeepSeek-V3 routing
+    (4096, 256, 8, 8, 4, "sigmoid", True, 3, 2.5),        # DeepSeek-V3 routing, ties
+    (1000, 16, 4, 4, 2, "sigmoid", True, 3, 1.0),
+    (7, 3, 3, 1, 1, "softmax", False, None, 1.0),         # k = E
+    (1, 1, 1, 1, 1, "sigmoid", False, None, 1.0),         # single expert
+    (333, 64, 6, 1, 1, "sigmoid", True, 4, 1.0),
+    (128, 1024, 32, 32, 8, "sigmoid", True, None, 2.5),   # largest E and k supported
+    (65, 40, 5, 1, 1, "softmax", False, 1, 1.7),          # E not a multiple of 32
+]
+
+
+@pytest.mark.parametrize("T,E,k,ng,tg,fn,use_bias,qb,scale", CASES)
+def test_route_from_scores_bit_exact(oracle, T, E, k, ng, tg, fn, use_bias, qb, scale):
+    scores = inputs.make_scores(T, E, fn, seed=T + E, quant_bits=qb, device="cuda")
+    bias = None
+    if use_bias:
+        g = torch.Generator(device="cuda")
+        g.manual_seed(E)
+        bias = torch.randn(E, generator=g, device="cuda") * 0.05
+        if qb is not None:
+            bias = torch.round(bias * 2 ** qb) / 2 ** qb
+    cfg = B.route_cfg(E, k, ng, tg, B.SIGMOID if fn == "sigmoid" else B.SOFTMAX, scale)
+    idx, w = cuda_i32((T, k)), cuda_f32((T, k))
+    B.moe_route_from_scores(scores, bias, cfg, idx, w)
+    torch.cuda.synchronize()
+    sc, bb = np_(scores), np_(bias)
+    ref_idx = oracle.select(sc, k, bias=bb, n_group=ng, topk_group=tg)
+    np.testing.assert_array_equal(np_(idx), ref_idx)
+    ref_w = oracle.gates(sc, ref_idx, oracle.SIGMOID if fn == "sigmoid" else oracle.SOFTMAX, scale)
+    np.testing.assert_allclose(np_(w), ref_w, rtol=GATE_RTOL, atol=1e-7)
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "mixtral_bf16", "dsv3_prefill", "dsv3_zipf"])
+def test_route_full_router(oracle, name):
+    """moe_route on the workload's own x and router weights: scores close to the
+    oracle's; expert choice identical except where the oracle's own margin is
+    below fp32 rounding of the scores."""
+    cfg = inputs.CONFIGS[name]
+    T = min(cfg.T, 2048)
+    inp = inputs.make_inputs(cfg.with_(T=T), seed=0, device="cuda", experts=False)
+    rc = B.cfg_from(cfg)
+    scores, idx, w = cuda_f32((T, cfg.E)), cuda_i32((T, cfg.k)), cuda_f32((T, cfg.k))
+    B.moe_route(inp["x"], inp["w_router"], inp["bias"], rc, scores, idx, w)
+    torch.cuda.synchronize()
+    fn = oracle.SIGMOID if cfg.score_fn == "sigmoid" else oracle.SOFTMAX
+    ref_sc = oracle.router_scores(np_(inp["x"]), np_(inp["w_router"]), fn)
+    np.testing.assert_allclose(np_(scores), ref_sc, rtol=1e-4, atol=2e-5)
+    bias = np_(inp["bias"])
+    ref_idx = oracle.select(ref_sc, cfg.k, bias=bias, n_group=cfg.n_group, topk_group=cfg.topk_group)
+    got = np_(idx)
+    differ = (got != ref_idx).any(1)
+    amb = near_tie_tokens(ref_sc, bias, cfg.k, cfg.n_group, cfg.topk_group, rel=1e-5)
+    assert not (differ & ~amb).any(), f"{int((differ & ~amb).sum())} tokens differ without a near tie"
+    assert differ.sum() <= max(2, T // 500)
