@@ -217,9 +217,10 @@ int moe_dispatch(const int32_t* topk_idx, const void* x, int dtype, int T, int d
     if (k < 1 || k > 32 || E < 1 || E > 1024) return E > 1024 ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
     int rc = check_dims(T, d, k);
     if (rc != MOE_OK) return rc;
-    if (!dtype_ok(dtype) || !topk_idx || !counts || !offsets || !slot_to_row || !row_to_token)
-        return MOE_ERR_INVALID_ARG;
-    if ((x_perm != nullptr) != (x != nullptr)) return MOE_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype) || !counts || !offsets) return MOE_ERR_INVALID_ARG;
+    // with no slots the per-slot arrays are empty and may be NULL
+    if (T > 0 && (!topk_idx || !slot_to_row || !row_to_token)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (x_perm != nullptr) != (x != nullptr)) return MOE_ERR_INVALID_ARG;
     if (x && (!moe_host::aligned16(x) || !moe_host::aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
     if (!ws || ws_bytes < moe_dispatch_workspace_size(T, k, E)) return MOE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

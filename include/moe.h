@@ -116,7 +116,8 @@ size_t moe_dispatch_workspace_size(int T, int k, int E);
  *   x_perm [S,d]     x_perm[row(s)] = x[s / k]  (dtype of x; may be NULL to
  *                    compute the index maps only)
  * topk_idx entries must lie in [0,E); others set the error word and leave
- * the outputs unspecified.  ws: moe_dispatch_workspace_size bytes, any
+ * the outputs unspecified.  With T = 0 only counts/offsets are written (zeros)
+ * and the per-slot pointers may be NULL.  ws: moe_dispatch_workspace_size bytes, any
  * contents; its first 16 bytes hold the error word (see moe_check_error). */
 int moe_dispatch(const int32_t* topk_idx, const void* x, int dtype, int T, int d, int k, int E,
                  int32_t* counts, int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_token,

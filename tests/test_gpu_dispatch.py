@@ -82,7 +82,7 @@ def test_dispatch_out_of_range_index_is_flagged():
     # The host cannot see device-side indices; the count kernel skips an index
     # outside [0, E), flags it in the error word and the permute stage is
     # skipped.  No out-of-bounds access happens.
-    idx = distinct_topk(100, 2, 8, seed=9)
+    idx = distinct_topk(100, 8, 2, seed=9)
     idx[17, 1] = 8
     rc, detail, *_ = run_dispatch(idx, torch.zeros((100, 16), dtype=torch.bfloat16, device="cuda"), 8)
     assert rc == B.ERR_DEVICE_INPUT and detail != 0
