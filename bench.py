@@ -37,9 +37,14 @@ L2_FLUSH_BYTES = 512 << 20
 LAUNCHES_PER_STEP_SHARED = 9
 LAUNCHES_PER_STEP_NOSHARED = 7
 
-# DRAM traffic of the routed gate/up GEMM per launch, from an ncu capture of
-# the same kernel source (see profiles/); None when the source has changed.
-TRAFFIC = {"source_sha256": None, "bytes_per_launch_at_workload": {}}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the routed
+# gate/up GEMM per launch, from one ncu capture of this kernel source on the
+# 32-expert workload, scaled x8 (experts and tokens) to the 256-expert layer
+# (profiles/grouped_gemm_tc_dsv3_prefill_e32.md).  Reported as null once the
+# kernel source no longer matches the captured one.
+TRAFFIC = {"source_sha256": "249a4017ed745cdd01a8c3cd64389efc3c0731e27db542ac4c058850f7b3d0d8",
+           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.961467e9,
+                                            "dsv3_prefill": 8 * 1.961467e9}}
 
 
 def peaks():

@@ -79,6 +79,9 @@ CONFIGS = {
     "dsv3_prefill": MoEConfig("dsv3_prefill", T=4096, **_DSV3),
     "dsv3_decode": MoEConfig("dsv3_decode", T=128, **_DSV3),
     "dsv3_zipf": MoEConfig("dsv3_zipf", T=16384, **{**_DSV3, "bias": "zipf"}),
+    # DeepSeek-V3 layer shapes with 32 experts and 512 tokens: the same ~128
+    # tokens per expert as dsv3_prefill in 1/8 of the memory (profiling case)
+    "dsv3_prefill_e32": MoEConfig("dsv3_prefill_e32", T=512, **{**_DSV3, "E": 32}),
 }
 
 
