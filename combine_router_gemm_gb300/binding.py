@@ -25,7 +25,7 @@ SOFTMAX, SIGMOID = 0, 1
 SYMBOLS = ("moe_status_string", "moe_version", "moe_route_from_scores", "moe_route",
            "moe_dispatch_workspace_size", "moe_dispatch", "moe_grouped_ffn_workspace_size",
            "moe_grouped_ffn", "moe_combine", "moe_layer_workspace_size", "moe_layer",
-           "moe_check_error")
+           "moe_check_error", "moe_dispatch_noalloc")
 
 
 class MoEError(RuntimeError):
@@ -89,6 +89,8 @@ def load() -> ctypes.CDLL:
     lib.moe_layer.restype = i32
     lib.moe_check_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
     lib.moe_check_error.restype = i32
+    lib.moe_dispatch_noalloc.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
+    lib.moe_dispatch_noalloc.restype = i32
     _lib = lib
     return lib
 
@@ -176,6 +178,30 @@ def moe_dispatch(topk_idx, x, E: int, counts, offsets, slot_to_row, row_to_token
                              _ptr(x_perm, None, "x_perm"), _ptr(ws, None, "ws"),
                              ws.numel() * ws.element_size(), _stream(stream))
     _check(rc, "moe_dispatch")
+
+
+DISPATCH_NOALLOC_MAX_SLOTS = 131072
+
+
+def moe_dispatch_noalloc(topk_idx, x, E: int, counts, offsets, slot_to_row, row_to_token, x_perm,
+                         device_error=None, stream=None):
+    """moe_dispatch without a workspace: for callers that may not allocate
+    device memory while they run (fixed memory pools, hosted plug-ins).  The
+    library keeps the scratch in a fixed device array of its own; calls must
+    not overlap on the GPU.  ``device_error``: optional int32 CUDA tensor of
+    one element that receives the call's error word."""
+    T, k = topk_idx.shape
+    d = x.shape[1] if x is not None else 8
+    dt = _dtype_code(x) if x is not None else BF16
+    rc = load().moe_dispatch_noalloc(_ptr(topk_idx, torch.int32, "topk_idx"), _ptr(x, None, "x"),
+                                     dt, T, d, k, E, _ptr(counts, torch.int32, "counts"),
+                                     _ptr(offsets, torch.int32, "offsets"),
+                                     _ptr(slot_to_row, torch.int32, "slot_to_row"),
+                                     _ptr(row_to_token, torch.int32, "row_to_token"),
+                                     _ptr(x_perm, None, "x_perm"),
+                                     _ptr(device_error, torch.int32, "device_error"),
+                                     _stream(stream))
+    _check(rc, "moe_dispatch_noalloc")
 
 
 def moe_grouped_ffn_workspace_size(rows: int, d: int, I: int, dtype: int) -> int:

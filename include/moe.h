@@ -193,6 +193,36 @@ size_t moe_layer_workspace_size(const moe_layer_args* a);
 int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, void* stream,
               void* stream2);
 
+/* ------------------------------------------------- allocation-free dispatch */
+
+/* Largest T*k that moe_dispatch_noalloc accepts (E up to 1024). */
+#define MOE_DISPATCH_NOALLOC_MAX_SLOTS 131072
+
+/* moe_dispatch for callers that cannot allocate device memory while they run
+ * (a serving runtime whose memory pool is fixed at start-up, a plug-in inside
+ * a framework that owns the allocator, code allowed to allocate only during
+ * initialisation).  The pages have no counterpart; this is a library
+ * convenience.  Same arguments and outputs as moe_dispatch, but no workspace:
+ * the scratch lives in a fixed 1 MiB array in the library's device memory,
+ * which every GPU that loads the library holds until the process exits.
+ *   - T*k above MOE_DISPATCH_NOALLOC_MAX_SLOTS or E above 1024 is refused
+ *     with MOE_ERR_UNSUPPORTED; nothing is enqueued.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current) and caches it; make that first
+ *     call before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents
+ *     (each call clears what must start at zero).  Calls that may overlap on
+ *     the GPU -- on different streams without ordering between them -- race
+ *     on it and give wrong results; order them.
+ *   - device_error: optional device pointer to one uint32 that receives, in
+ *     stream order, this call's error word (0 = no error; otherwise the bits
+ *     moe_check_error would report).  NULL skips it.
+ *   - Calls no allocating function (no cudaMalloc/cudaFree or equivalent). */
+int moe_dispatch_noalloc(const int32_t* topk_idx, const void* x, int dtype, int T, int d, int k,
+                         int E, int32_t* counts, int32_t* offsets, int32_t* slot_to_row,
+                         int32_t* row_to_token, void* x_perm, uint32_t* device_error,
+                         void* stream);
+
 /* Synchronises `stream`, reads and clears the error word of `ws` (a workspace
  * previously passed to moe_dispatch / moe_grouped_ffn / moe_layer).  Returns
  * MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_INPUT or MOE_ERR_CUDA.  `detail`
