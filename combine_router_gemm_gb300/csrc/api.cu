@@ -8,11 +8,6 @@
 
 #include "common.cuh"
 
-namespace moe_tc {
-int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
-                     const void* w13, const void* w2, float* y, void* h, uint32_t* err,
-                     cudaStream_t s, cudaEvent_t between = nullptr);
-}
 namespace moe_f32 {
 int grouped_ffn_f32(const float* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
                     const float* w13, const float* w2, float* y, float* h, const uint32_t* err,
@@ -87,6 +82,20 @@ int run_ffn(const void* x_perm, const int32_t* offsets, int E, int rows, int d, 
     return rc;
 }
 
+size_t route_ws(int E, int d, int dtype) {
+    return ERR_BYTES + (dtype == MOE_BF16 ? al(moe_tc::router_ws_bytes(E, d)) : 0);
+}
+
+// bf16 activations: tcgen05 GEMM against the fp32 router weight split into
+// three bf16 terms; fp32 activations: fp32 CUDA-core GEMM.
+int run_router(const void* x, int dtype, const float* w_router, int T, int d, int E, int score_fn,
+               float* scores, void* wsplit, uint32_t* err, cudaStream_t s) {
+    if (dtype == MOE_BF16)
+        return moe_tc::router_bf16(x, w_router, T, d, E, score_fn == MOE_SCORE_SIGMOID, scores,
+                                   wsplit, err, s);
+    return moe_launch::router_gemm(x, dtype, w_router, T, d, E, score_fn, scores, s);
+}
+
 struct LayerWs {
     uint32_t* err;
     float* scores;
@@ -102,6 +111,7 @@ struct LayerWs {
     float* ysh;
     void* hsh;
     void* disp;
+    void* wsplit;
     size_t total;
 };
 
@@ -131,6 +141,7 @@ LayerWs carve_layer(const moe_layer_args* a, void* base) {
     w.ysh = sh ? static_cast<float*>(take((size_t)T * d * 4)) : nullptr;
     w.hsh = sh ? take((size_t)T * a->I_sh * es) : nullptr;
     w.disp = take(moe_launch::dispatch_ws_bytes(T, k, E));
+    w.wsplit = a->dtype == MOE_BF16 ? take(moe_tc::router_ws_bytes(E, d)) : nullptr;
     w.total = off;
     return w;
 }
@@ -188,9 +199,14 @@ int moe_route_from_scores(const float* scores, const float* bias, int T, const m
                             static_cast<cudaStream_t>(stream));
 }
 
+size_t moe_route_workspace_size(int E, int d, int dtype) {
+    if (E < 1 || d < 1 || !dtype_ok(dtype)) return 0;
+    return route_ws(E, d, dtype);
+}
+
 int moe_route(const void* x, int dtype, const float* w_router, const float* bias, int T, int d,
-              const moe_route_cfg* cfg, float* scores, int32_t* topk_idx, float* topk_w,
-              void* stream) {
+              const moe_route_cfg* cfg, float* scores, int32_t* topk_idx, float* topk_w, void* ws,
+              size_t ws_bytes, void* stream) {
     int rc = check_cfg(cfg);
     if (rc != MOE_OK) return rc;
     if ((rc = check_dims(T, d, cfg->top_k)) != MOE_OK) return rc;
@@ -198,10 +214,14 @@ int moe_route(const void* x, int dtype, const float* w_router, const float* bias
         return MOE_ERR_INVALID_ARG;
     if (!moe_host::aligned16(x) || !moe_host::aligned16(w_router)) return MOE_ERR_INVALID_ARG;
     if (bias && cfg->score_fn == MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
-    if (T == 0) return MOE_OK;
+    if (!ws || !moe_host::aligned16(ws) || ws_bytes < route_ws(cfg->num_experts, d, dtype))
+        return MOE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    rc = moe_launch::router_gemm(x, dtype, w_router, T, d, cfg->num_experts, cfg->score_fn, scores,
-                                 s);
+    uint32_t* err = static_cast<uint32_t*>(ws);
+    if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (T == 0) return MOE_OK;
+    rc = run_router(x, dtype, w_router, T, d, cfg->num_experts, cfg->score_fn, scores,
+                    static_cast<char*>(ws) + ERR_BYTES, err, s);
     if (rc != MOE_OK) return rc;
     return moe_launch::topk(scores, bias, T, cfg, topk_idx, topk_w, s);
 }
@@ -298,8 +318,14 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
         if (rc == MOE_OK && stage[i] && cudaEventRecord(stage[i], s0) != cudaSuccess) rc = MOE_ERR_CUDA;
     };
     mark(0);
+    // bf16 with a shared expert of the routed experts' size: the shared expert
+    // runs inside the routed grouped-GEMM launches (its compute-bound tiles
+    // interleaved with the weight-streaming ones).  Otherwise it runs as its
+    // own launches, on stream2 when given.
+    const bool merged = sh && a->dtype == MOE_BF16 && a->I_sh == I;
+    moe_tc::SharedExpert shx{a->x, T, a->w13_sh, a->w2_sh, w.hsh, w.ysh};
     cudaEvent_t ev_start = nullptr, ev_shared = nullptr;
-    const bool overlap = sh && s1 && s1 != s0;
+    const bool overlap = sh && !merged && s1 && s1 != s0;
     if (overlap) {
         if (cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&ev_shared, cudaEventDisableTiming) != cudaSuccess)
@@ -313,8 +339,8 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
         if (rc == MOE_OK && cudaEventRecord(ev_shared, s1) != cudaSuccess) rc = MOE_ERR_CUDA;
     }
     if (rc == MOE_OK)
-        rc = moe_launch::router_gemm(a->x, a->dtype, a->w_router, T, d, E, a->route.score_fn,
-                                     w.scores, s0);
+        rc = run_router(a->x, a->dtype, a->w_router, T, d, E, a->route.score_fn, w.scores, w.wsplit,
+                        w.err, s0);
     mark(1);
     if (rc == MOE_OK) rc = moe_launch::topk(w.scores, a->bias, T, &a->route, w.idx, w.w, s0);
     mark(2);
@@ -322,11 +348,16 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
         rc = moe_launch::dispatch(w.idx, a->x, a->dtype, T, d, k, E, w.counts, w.offsets, w.s2r,
                                   w.r2t, w.xp, w.disp, w.err, s0);
     mark(3);
-    if (rc == MOE_OK)
-        rc = run_ffn(w.xp, w.offsets, E, T * k, d, I, a->w13, a->w2, a->dtype, w.yp, w.h, w.err, s0,
-                     stage[4]);
+    if (rc == MOE_OK) {
+        if (merged)
+            rc = moe_tc::grouped_ffn_bf16(w.xp, w.offsets, E, T * k, d, I, a->w13, a->w2, w.yp, w.h,
+                                          w.err, s0, stage[4], &shx);
+        else
+            rc = run_ffn(w.xp, w.offsets, E, T * k, d, I, a->w13, a->w2, a->dtype, w.yp, w.h,
+                         w.err, s0, stage[4]);
+    }
     mark(5);
-    if (rc == MOE_OK && sh && !overlap)
+    if (rc == MOE_OK && sh && !merged && !overlap)
         rc = run_ffn(a->x, nullptr, 1, T, d, a->I_sh, a->w13_sh, a->w2_sh, a->dtype, w.ysh, w.hsh,
                      w.err, s0);
     if (rc == MOE_OK && overlap && cudaStreamWaitEvent(s0, ev_shared, 0) != cudaSuccess)

@@ -57,6 +57,27 @@ int launch_status();  // MOE_OK or MOE_ERR_CUDA after a launch
 int num_sms();
 }  // namespace moe_host
 
+// ---- tcgen05 kernels (grouped_gemm_tc.cu) ----------------------------------
+namespace moe_tc {
+// A second, dense problem run inside the same grouped-GEMM launches: the
+// shared expert over all T tokens (same I as the routed experts).
+struct SharedExpert {
+    const void* x;    // [T,d] bf16
+    int T;
+    const void* w13;  // [2I,d]
+    const void* w2;   // [d,I]
+    void* h;          // [T,I] bf16 scratch
+    float* y;         // [T,d] fp32 out
+};
+int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
+                     const void* w13, const void* w2, float* y, void* h, uint32_t* err,
+                     cudaStream_t s, cudaEvent_t between = nullptr,
+                     const SharedExpert* sh = nullptr);
+size_t router_ws_bytes(int E, int d);
+int router_bf16(const void* x, const float* w_router, int T, int d, int E, int sigmoid,
+                float* scores, void* ws, uint32_t* err, cudaStream_t s);
+}  // namespace moe_tc
+
 // ---- internal launchers (one per kernel family), used by api.cu -----------
 namespace moe_launch {
 int router_gemm(const void* x, int dtype, const float* w_router, int T, int d, int E, int score_fn,

@@ -33,34 +33,47 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace {
 
 constexpr int BM = 128;         // features per tile (MMA M)
 constexpr int BK = 64;          // K per stage: one 128-byte swizzle atom row
-constexpr int BN_MAX = 256;     // tokens per tile (MMA N upper bound)
 constexpr int B_BOX = 32;       // token rows per TMA box
 constexpr int A_TILE_BYTES = BM * BK * 2;      // 16 KB
-constexpr int B_TILE_BYTES = BN_MAX * BK * 2;  // 32 KB
 constexpr int B_BOX_BYTES = B_BOX * BK * 2;    // 4 KB
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 1024;
 
+// MODE 0: gate/up + SwiGLU (W1 and W3 tiles into two accumulators)
+// MODE 1: down projection (one A tile, double-buffered accumulator)
+// MODE 2: router, fp32 weight split into three bf16 terms (hi, mid, lo)
+//         that all accumulate into one accumulator
 template <int MODE>
 struct Cfg;
 template <>
-struct Cfg<0> {  // gate/up + SwiGLU: two A tiles (W1, W3) per stage
-    static constexpr int NUM_A = 2, STAGES = 3, ACC_STAGES = 1;
+struct Cfg<0> {
+    static constexpr int NUM_A = 2, STAGES = 3, ACC_STAGES = 1, BN = 256;
+    static constexpr bool SPLIT_ACC = true;  // one accumulator per A tile
 };
 template <>
-struct Cfg<1> {  // down: one A tile per stage, double-buffered accumulator
-    static constexpr int NUM_A = 1, STAGES = 4, ACC_STAGES = 2;
+struct Cfg<1> {
+    static constexpr int NUM_A = 1, STAGES = 4, ACC_STAGES = 2, BN = 256;
+    static constexpr bool SPLIT_ACC = false;
+};
+template <>
+struct Cfg<2> {
+    static constexpr int NUM_A = 3, STAGES = 3, ACC_STAGES = 2, BN = 64;
+    static constexpr bool SPLIT_ACC = false;
 };
 
 template <int MODE>
-__host__ __device__ constexpr int stage_bytes() { return Cfg<MODE>::NUM_A * A_TILE_BYTES + B_TILE_BYTES; }
+__host__ __device__ constexpr int stage_bytes() {
+    return Cfg<MODE>::NUM_A * A_TILE_BYTES + Cfg<MODE>::BN * BK * 2;
+}
 
 template <int MODE>
 __host__ __device__ constexpr size_t smem_bytes() {
@@ -75,9 +88,14 @@ struct Params {
     int K;                   // reduction length
     int N_out;               // output features per expert
     int a_rows;              // weight rows per expert in the 2D weight view
-    int up_off;              // row offset of W3 inside an expert (gate/up only)
-    void* out;               // H bf16 [rows, N_out] or Y fp32 [rows, N_out]
+    int a_step;              // row distance between the A tiles of one stage
+    void* out;               // H bf16 / Y fp32 / scores fp32, [rows, N_out]
     uint32_t* err;
+    int flags;               // router: bit 0 = apply sigmoid
+    // optional second problem run in the same launch (the shared expert): one
+    // dense segment of `rows2` rows through tm_a2/tm_b2 into out2
+    int rows2;
+    void* out2;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -203,16 +221,36 @@ __device__ __forceinline__ void tmem_wait_ld() {
 // ---------------------------------------------------------------- schedule
 
 struct Unit {
-    int e;        // expert
+    int e;        // expert (E for the second, dense problem)
     int m_start;  // first activation row of the token tile
-    int n_tok;    // tokens in the tile (1..256)
+    int n_tok;    // tokens in the tile (1..BN)
     int n0;       // first output feature
+    bool second;  // unit of the second problem (shared expert)
 };
 
-// Units of expert e occupy [mpre[e] * nt, mpre[e+1] * nt); inside, the feature
-// tile is the major index and the token tile the minor one.
+// Routed units of expert e occupy [mpre[e] * nt, mpre[e+1] * nt); inside, the
+// feature tile is the major index and the token tile the minor one.  Units of
+// the second problem (U2 of them) are spread evenly through the sequence: with
+// period P = U / U2, position j*P holds second-problem unit j.
+template <int BN>
 __device__ __forceinline__ Unit decode_unit(int u, const int* mpre, const int* offs, int E,
-                                            int n_tiles) {
+                                            int n_tiles, int U, int U2, int rows2) {
+    Unit r;
+    if (U2 > 0) {
+        const int P = U / U2;
+        const int j = u / P;
+        if (u - j * P == 0 && j < U2) {
+            const int mt2 = (rows2 + BN - 1) / BN;
+            const int nt = j / mt2, mtile = j - nt * mt2;
+            r.e = E;
+            r.second = true;
+            r.m_start = mtile * BN;
+            r.n_tok = min(BN, rows2 - r.m_start);
+            r.n0 = nt * BM;
+            return r;
+        }
+        u -= min(U2, j + 1);
+    }
     int lo = 0, hi = E;  // find e with mpre[e]*nt <= u < mpre[e+1]*nt
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -222,10 +260,10 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* mpre, const int* o
     const int mt = mpre[e + 1] - mpre[e];
     const int local = u - mpre[e] * n_tiles;
     const int nt = local / mt, mtile = local - nt * mt;
-    Unit r;
     r.e = e;
-    r.m_start = offs[e] + mtile * BN_MAX;
-    r.n_tok = min(BN_MAX, offs[e + 1] - r.m_start);
+    r.second = false;
+    r.m_start = offs[e] + mtile * BN;
+    r.n_tok = min(BN, offs[e + 1] - r.m_start);
     r.n0 = nt * BM;
     return r;
 }
@@ -235,9 +273,13 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* mpre, const int* o
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a,
-                           const __grid_constant__ CUtensorMap tm_b, const Params p) {
+                           const __grid_constant__ CUtensorMap tm_b,
+                           const __grid_constant__ CUtensorMap tm_a2,
+                           const __grid_constant__ CUtensorMap tm_b2, const Params p) {
     using C = Cfg<MODE>;
-    constexpr int STAGES = C::STAGES, NUM_A = C::NUM_A, ACC = C::ACC_STAGES;
+    constexpr int STAGES = C::STAGES, NUM_A = C::NUM_A, ACC = C::ACC_STAGES, BN = C::BN;
+    constexpr int ACC_COLS = C::SPLIT_ACC ? NUM_A * BN : BN;  // TMEM columns per accumulator stage
+    static_assert(ACC * ACC_COLS <= TMEM_COLS, "accumulators exceed tensor memory");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -253,12 +295,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* total_units = reinterpret_cast<int*>(tmem_slot + 2);
     int* mpre = reinterpret_cast<int*>(smem + (size_t)STAGES * stage_bytes<MODE>() + 256);
-    // offsets are re-read from global (read-only, L1/L2 resident)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // ---- schedule: token tiles per expert and their prefix (warp 0) -------
     const int E = p.E;
     const int n_tiles = (p.N_out + BM - 1) / BM;
+    const int U2 = p.rows2 > 0 ? ((p.rows2 + BN - 1) / BN) * n_tiles : 0;
     if (warp == 0) {
         // per-lane chunk of experts, then a warp scan of the chunk sums
         const int per = (E + 31) / 32;
@@ -269,7 +311,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int a = p.offsets ? p.offsets[e] : 0;
             const int b = p.offsets ? p.offsets[e + 1] : p.rows;
             if (a < 0 || b < a || b > p.rows) bad = true;
-            sum += (b - a + BN_MAX - 1) / BN_MAX;
+            sum += (b - a + BN - 1) / BN;
         }
         int inc = sum;
 #pragma unroll
@@ -282,13 +324,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mpre[e] = run;
             const int a = p.offsets ? p.offsets[e] : 0;
             const int b = p.offsets ? p.offsets[e + 1] : p.rows;
-            run += (b - a + BN_MAX - 1) / BN_MAX;
+            run += (b - a + BN - 1) / BN;
         }
         const bool any_bad = __any_sync(0xffffffffu, bad);
         if (lane == 31) {
             mpre[E] = inc;
             // an earlier stage that failed, or inconsistent offsets: no work
-            *total_units = (any_bad || moe::read_error(p.err)) ? -1 : inc * n_tiles;
+            *total_units = (any_bad || moe::read_error(p.err)) ? -1 : inc * n_tiles + U2;
             if (any_bad) moe::raise_error(p.err, moe::ERR_BAD_OFFSETS);
         }
     }
@@ -306,6 +348,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
+        if (p.rows2 > 0) {
+            tma_prefetch_desc(&tm_a2);
+            tma_prefetch_desc(&tm_b2);
+        }
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -337,10 +383,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             long issued = 0;
             for (int u = blockIdx.x; u < U && !*abort_flag; u += gridDim.x) {
-                const Unit t = decode_unit(u, mpre, offs, E, n_tiles);
+                const Unit t = decode_unit<BN>(u, mpre, offs, E, n_tiles, U, U2, p.rows2);
+                const CUtensorMap* ma = t.second ? &tm_a2 : &tm_a;
+                const CUtensorMap* mb = t.second ? &tm_b2 : &tm_b;
                 const int nbox = (t.n_tok + B_BOX - 1) / B_BOX;
                 const uint32_t bytes = NUM_A * A_TILE_BYTES + nbox * B_BOX_BYTES;
-                const int a_row = t.e * p.a_rows + t.n0;
+                const int a_row = (t.second ? 0 : t.e * p.a_rows) + t.n0;
                 bool ok = true;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, p.err,
@@ -352,11 +400,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t fb = smem_u32(&full_bar[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
                     const int kx = kb * BK;
-                    tma_load_2d(smem_u32(st), &tm_a, fb, kx, a_row);
-                    if (NUM_A == 2) tma_load_2d(smem_u32(st + A_TILE_BYTES), &tm_a, fb, kx, a_row + p.up_off);
+#pragma unroll
+                    for (int a = 0; a < NUM_A; ++a)
+                        tma_load_2d(smem_u32(st + a * A_TILE_BYTES), ma, fb, kx, a_row + a * p.a_step);
                     uint8_t* bdst = st + NUM_A * A_TILE_BYTES;
                     for (int j = 0; j < nbox; ++j)
-                        tma_load_2d(smem_u32(bdst + j * B_BOX_BYTES), &tm_b, fb, kx,
+                        tma_load_2d(smem_u32(bdst + j * B_BOX_BYTES), mb, fb, kx,
                                     t.m_start + j * B_BOX);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -384,14 +433,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t acc_phase = 0;
             bool issued_any = false;
             for (int u = blockIdx.x; u < U && !*abort_flag; u += gridDim.x) {
-                const Unit t = decode_unit(u, mpre, offs, E, n_tiles);
+                const Unit t = decode_unit<BN>(u, mpre, offs, E, n_tiles, U, U2, p.rows2);
                 const int bn = (t.n_tok + 15) & ~15;
                 const uint32_t idesc = idesc_bf16(bn);
                 if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, abort_flag, p.err,
                                moe::WAIT_LIMIT_NS))
                     break;
                 tc_fence_after();
-                const uint32_t d0 = tmem_base + (uint32_t)(acc * 256);
+                const uint32_t d0 = tmem_base + (uint32_t)(acc * ACC_COLS);
                 bool ok = true;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(smem_u32(&full_bar[stage]), phase, abort_flag, p.err,
@@ -405,11 +454,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         const uint64_t bdesc = smem_desc_sw128(bsm + kk * 32);
-                        const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-                        mma_bf16(d0, smem_desc_sw128(st + kk * 32), bdesc, idesc, accum);
-                        if (NUM_A == 2)
-                            mma_bf16(d0 + 256, smem_desc_sw128(st + A_TILE_BYTES + kk * 32), bdesc,
-                                     idesc, accum);
+#pragma unroll
+                        for (int a = 0; a < NUM_A; ++a) {
+                            const uint32_t dst = C::SPLIT_ACC ? d0 + (uint32_t)(a * BN) : d0;
+                            // the first product into an accumulator overwrites it
+                            const bool first = kb == 0 && kk == 0 && (C::SPLIT_ACC || a == 0);
+                            mma_bf16(dst, smem_desc_sw128(st + a * A_TILE_BYTES + kk * 32), bdesc,
+                                     idesc, first ? 0u : 1u);
+                        }
                     }
                     issued_any = true;
                     mma_commit(smem_u32(&empty_bar[stage]));  // frees the stage when done
@@ -434,22 +486,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < U; u += gridDim.x) {
-            const Unit t = decode_unit(u, mpre, offs, E, n_tiles);
+            const Unit t = decode_unit<BN>(u, mpre, offs, E, n_tiles, U, U2, p.rows2);
             if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.err,
                            moe::WAIT_LIMIT_NS))
                 break;
             tc_fence_after();
             const int n = t.n0 + q * 32 + lane;
             const bool n_ok = n < p.N_out;
-            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 256);
+            void* out = t.second ? p.out2 : p.out;
+            const uint32_t tbase =
+                tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
             for (int c0 = 0; c0 < t.n_tok; c0 += 32) {
                 uint32_t g[32];
                 tmem_ld32(tbase + c0, g);
                 if (MODE == 0) {
                     uint32_t up[32];
-                    tmem_ld32(tbase + 256 + c0, up);
+                    tmem_ld32(tbase + BN + c0, up);
                     tmem_wait_ld();
-                    __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out);
+                    __nv_bfloat16* H = static_cast<__nv_bfloat16*>(out);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int tok = c0 + j;
@@ -462,12 +516,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 } else {
                     tmem_wait_ld();
-                    float* Y = static_cast<float*>(p.out);
+                    float* Y = static_cast<float*>(out);
+                    const bool sig = MODE == 2 && (p.flags & 1);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int tok = c0 + j;
-                        if (n_ok && tok < t.n_tok)
-                            Y[(size_t)(t.m_start + tok) * p.N_out + n] = __uint_as_float(g[j]);
+                        if (n_ok && tok < t.n_tok) {
+                            float v = __uint_as_float(g[j]);
+                            if (sig) v = 1.0f / (1.0f + expf(-v));
+                            Y[(size_t)(t.m_start + tok) * p.N_out + n] = v;
+                        }
                     }
                 }
             }
@@ -485,6 +543,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                      "r"(TMEM_COLS)
                      : "memory");
+    }
+}
+
+// Router weight split: w = hi + mid + lo with each term the bf16 rounding of
+// what the previous terms leave (every subtraction is exact in fp32).
+__global__ void split_weight_kernel(const float* __restrict__ w, long n,
+                                    __nv_bfloat16* __restrict__ out) {
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n;
+         i += (long)gridDim.x * blockDim.x) {
+        const float v = w[i];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const float r1 = v - __bfloat162float(hi);
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const float r2 = r1 - __bfloat162float(mid);
+        out[i] = hi;
+        out[n + i] = mid;
+        out[2 * n + i] = __float2bfloat16_rn(r2);
     }
 }
 
@@ -520,7 +595,8 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 }
 
 template <int MODE>
-int launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t s) {
+int launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& a2,
+           const CUtensorMap& b2, const Params& p, cudaStream_t s) {
     static bool attr_done = false;
     const size_t smem = smem_bytes<MODE>();
     if (!attr_done) {
@@ -530,7 +606,7 @@ int launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStre
             return MOE_ERR_CUDA;
         attr_done = true;
     }
-    grouped_gemm_tc_kernel<MODE><<<moe_host::num_sms(), NUM_THREADS, smem, s>>>(a, b, p);
+    grouped_gemm_tc_kernel<MODE><<<moe_host::num_sms(), NUM_THREADS, smem, s>>>(a, b, a2, b2, p);
     return moe_host::launch_status();
 }
 
@@ -539,23 +615,50 @@ int launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStre
 namespace moe_tc {
 
 // Both GEMMs of the SwiGLU FFN over bf16 rows; offsets == NULL means one
-// segment [0, rows) with expert 0 (dense, e.g. the shared expert).
+// segment [0, rows) with expert 0 (dense).  When sh is given, the shared
+// expert (dense over sh->x, I_sh == I) runs inside the same two launches.
 int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
                      const void* w13, const void* w2, float* y, void* h, uint32_t* err,
-                     cudaStream_t s, cudaEvent_t between) {
+                     cudaStream_t s, cudaEvent_t between, const SharedExpert* sh) {
     if (E > MAX_E) return MOE_ERR_UNSUPPORTED;
-    CUtensorMap a1, b1, a2, b2;
+    CUtensorMap a1, b1, a2, b2, a1s, b1s, a2s, b2s;
     if (!make_map(&a1, w13, (uint64_t)E * 2 * I, d, BM) ||
         !make_map(&b1, x_perm, rows, d, B_BOX) ||
         !make_map(&a2, w2, (uint64_t)E * d, I, BM) ||
         !make_map(&b2, h, rows, I, B_BOX))
         return MOE_ERR_CUDA;
-    Params p1{offsets, E, rows, d, I, 2 * I, I, h, err};
-    int rc = launch<0>(a1, b1, p1, s);
+    const bool two = sh != nullptr && sh->T > 0;
+    if (two) {
+        if (!make_map(&a1s, sh->w13, 2ull * I, d, BM) || !make_map(&b1s, sh->x, sh->T, d, B_BOX) ||
+            !make_map(&a2s, sh->w2, (uint64_t)d, I, BM) || !make_map(&b2s, sh->h, sh->T, I, B_BOX))
+            return MOE_ERR_CUDA;
+    } else {
+        a1s = a1; b1s = b1; a2s = a2; b2s = b2;
+    }
+    Params p1{offsets, E, rows, d, I, 2 * I, I, h, err, 0, two ? sh->T : 0, two ? sh->h : nullptr};
+    int rc = launch<0>(a1, b1, a1s, b1s, p1, s);
     if (rc != MOE_OK) return rc;
     if (between && cudaEventRecord(between, s) != cudaSuccess) return MOE_ERR_CUDA;
-    Params p2{offsets, E, rows, I, d, d, 0, y, err};
-    return launch<1>(a2, b2, p2, s);
+    Params p2{offsets, E, rows, I, d, d, 0, y, err, 0, two ? sh->T : 0, two ? sh->y : nullptr};
+    return launch<1>(a2, b2, a2s, b2s, p2, s);
+}
+
+size_t router_ws_bytes(int E, int d) { return (size_t)3 * E * d * 2; }
+
+// scores[T,E] = x W^T (fp32 accumulate) with W split into three bf16 terms;
+// sigmoid applied in the epilogue when asked.  ws: router_ws_bytes(E, d).
+int router_bf16(const void* x, const float* w_router, int T, int d, int E, int sigmoid,
+                float* scores, void* ws, uint32_t* err, cudaStream_t s) {
+    __nv_bfloat16* wsplit = static_cast<__nv_bfloat16*>(ws);
+    const long n = (long)E * d;
+    const int blocks = (int)std::min<long>((n + 255) / 256, 4L * moe_host::num_sms());
+    split_weight_kernel<<<blocks, 256, 0, s>>>(w_router, n, wsplit);
+    int rc = moe_host::launch_status();
+    if (rc != MOE_OK) return rc;
+    CUtensorMap a, b;
+    if (!make_map(&a, wsplit, 3ull * E, d, BM) || !make_map(&b, x, T, d, B_BOX)) return MOE_ERR_CUDA;
+    Params p{nullptr, 1, T, d, E, 0, E, scores, err, sigmoid ? 1 : 0, 0, nullptr};
+    return launch<2>(a, b, a, b, p, s);
 }
 
 }  // namespace moe_tc

@@ -15,25 +15,15 @@ namespace {
 
 // ---------------------------------------------------------------- router GEMM
 //
-// logits[t,e] = sum_i x[t,i] * W[e,i] on the CUDA cores in fp32 (the router is
-// fp32; it is 0.5% of the layer's flops).  Block tile 64 tokens x 64 experts,
-// K chunk 32; 256 threads, each owning a 4x4 block of outputs.
+// logits[t,e] = sum_i x[t,i] * W[e,i] on the CUDA cores in fp32, for fp32
+// activations (bf16 activations use the tensor-core router in
+// grouped_gemm_tc.cu).  Block tile 64 tokens x 64 experts, K chunk 32; 256
+// threads, each owning a 4x4 block of outputs.
 
 constexpr int RT_T = 64, RT_E = 64, RT_K = 32;
 
 template <typename XT>
 __device__ __forceinline__ void load_x8(const XT* p, float (&v)[8]);
-template <>
-__device__ __forceinline__ void load_x8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
-    uint4 u = *reinterpret_cast<const uint4*>(p);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 f = __bfloat1622float2(h[i]);
-        v[2 * i] = f.x;
-        v[2 * i + 1] = f.y;
-    }
-}
 template <>
 __device__ __forceinline__ void load_x8<float>(const float* p, float (&v)[8]) {
     float4 a = *reinterpret_cast<const float4*>(p);
@@ -267,14 +257,12 @@ namespace moe_launch {
 
 int router_gemm(const void* x, int dtype, const float* w_router, int T, int d, int E, int score_fn,
                 float* scores, cudaStream_t s) {
+    // fp32 activations only; bf16 activations take the tensor-core router
+    if (dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
     dim3 grid(moe::ceil_div(E, RT_E), moe::ceil_div(T, RT_T));
     const int sig = score_fn == MOE_SCORE_SIGMOID;
-    if (dtype == MOE_BF16)
-        router_gemm_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-            static_cast<const __nv_bfloat16*>(x), w_router, T, d, E, sig, scores);
-    else
-        router_gemm_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x), w_router, T,
-                                                       d, E, sig, scores);
+    router_gemm_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x), w_router, T, d, E,
+                                                   sig, scores);
     return moe_host::launch_status();
 }
 

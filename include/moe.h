@@ -94,13 +94,21 @@ int moe_route_from_scores(const float* scores, const float* bias, int T,
                           const moe_route_cfg* cfg, int32_t* topk_idx, float* topk_w,
                           void* stream);
 
+/* Workspace bytes moe_route needs (E experts, hidden size d). */
+size_t moe_route_workspace_size(int E, int d, int dtype);
+
 /* Router GEMM then moe_route_from_scores.
  *   x        [T,d] bf16 or fp32 (dtype)
  *   w_router [E,d] fp32
- *   scores   [T,E] fp32 out (logits, or sigmoid(logits)); fp32 accumulate */
+ *   scores   [T,E] fp32 out (logits, or sigmoid(logits)); fp32 accumulate
+ * bf16 x: tcgen05 tensor cores, with w_router split into three bf16 terms
+ * (hi + mid + lo, each the bf16 rounding of what the previous leave) so that
+ * every product is exact and sums are fp32 -- the result matches an fp32
+ * GEMM to fp32 rounding.  fp32 x: CUDA cores in fp32.
+ * ws: moe_route_workspace_size bytes (error word, split weight). */
 int moe_route(const void* x, int dtype, const float* w_router, const float* bias, int T, int d,
-              const moe_route_cfg* cfg, float* scores, int32_t* topk_idx, float* topk_w,
-              void* stream);
+              const moe_route_cfg* cfg, float* scores, int32_t* topk_idx, float* topk_w, void* ws,
+              size_t ws_bytes, void* stream);
 
 /* --------------------------------------------------------------- dispatch */
 
@@ -186,10 +194,11 @@ typedef struct {
 size_t moe_layer_workspace_size(const moe_layer_args* a);
 
 /* out [T,d] fp32 = the layer: route, dispatch, grouped FFN, shared expert,
- * combine.  `stream2` (may be NULL) is a second stream of the same device:
- * when given, the shared expert runs on it concurrently with the routed path,
- * ordered by events; everything is complete on `stream` when the call's work
- * finishes there. */
+ * combine.  With bf16 and I_sh == I the shared expert's tiles run inside the
+ * routed grouped-GEMM launches.  Otherwise `stream2` (may be NULL), a second
+ * stream of the same device, runs the shared expert concurrently with the
+ * routed path, ordered by events; everything is complete on `stream` when
+ * the call's work finishes there. */
 int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, void* stream,
               void* stream2);
 

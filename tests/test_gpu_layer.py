@@ -70,6 +70,10 @@ SMALL_BF16 = [
                      shared_I=128, bias="normal", expert_std=0.06, router_std=0.06),
     inputs.MoEConfig("small_mixtral", T=513, d=384, E=8, k=2, I=256, dtype="bf16",
                      expert_std=0.05),
+    # shared expert wider than the routed ones: separate launches (second stream)
+    inputs.MoEConfig("small_dsv3_wide_shared", T=300, d=256, E=16, k=4, I=128, dtype="bf16",
+                     score_fn="sigmoid", n_group=4, topk_group=2, routed_scale=2.5,
+                     shared_I=256, bias="normal", expert_std=0.06, router_std=0.06),
 ]
 
 

@@ -71,3 +71,23 @@ def test_route_full_router(oracle, name):
     amb = near_tie_tokens(ref_sc, bias, cfg.k, cfg.n_group, cfg.topk_group, rel=1e-5)
     assert not (differ & ~amb).any(), f"{int((differ & ~amb).sum())} tokens differ without a near tie"
     assert differ.sum() <= max(2, T // 500)
+
+
+@pytest.mark.parametrize("T,d,E,fn", [(333, 200, 40, "sigmoid"), (1, 64, 8, "softmax"),
+                                      (1000, 1024, 130, "softmax"), (257, 7168, 256, "sigmoid")])
+def test_router_tensor_core_split_weight(oracle, T, d, E, fn):
+    """bf16 activations: the tensor-core router with the fp32 weight split into
+    three bf16 terms matches the oracle's router to fp32 rounding (tails in
+    tokens, experts and K included)."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(T + d + E)
+    x = torch.randn((T, d), generator=g, device="cuda").to(torch.bfloat16)
+    wr = torch.randn((E, d), generator=g, device="cuda") * (d ** -0.5)
+    k = min(4, E)
+    cfg = B.route_cfg(E, k, 1, 1, B.SIGMOID if fn == "sigmoid" else B.SOFTMAX, 1.0)
+    scores, idx, w = cuda_f32((T, E)), cuda_i32((T, k)), cuda_f32((T, k))
+    B.moe_route(x, wr, None, cfg, scores, idx, w)
+    torch.cuda.synchronize()
+    ofn = oracle.SIGMOID if fn == "sigmoid" else oracle.SOFTMAX
+    ref = oracle.router_scores(np_(x), np_(wr), ofn)
+    np.testing.assert_allclose(np_(scores), ref, rtol=2e-6, atol=2e-6)
