@@ -26,7 +26,7 @@ SYMBOLS = ("moe_status_string", "moe_version", "moe_route_from_scores", "moe_rou
            "moe_route_workspace_size",
            "moe_dispatch_workspace_size", "moe_dispatch", "moe_grouped_ffn_workspace_size",
            "moe_grouped_ffn", "moe_combine", "moe_layer_workspace_size", "moe_layer",
-           "moe_check_error", "moe_dispatch_noalloc")
+           "moe_check_error", "moe_dispatch_noalloc", "moe_selftest_bounded_wait")
 
 
 class MoEError(RuntimeError):
@@ -94,6 +94,8 @@ def load() -> ctypes.CDLL:
     lib.moe_check_error.restype = i32
     lib.moe_dispatch_noalloc.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
     lib.moe_dispatch_noalloc.restype = i32
+    lib.moe_selftest_bounded_wait.argtypes = [i32, ctypes.c_uint32, P, sz, P]
+    lib.moe_selftest_bounded_wait.restype = i32
     _lib = lib
     return lib
 
@@ -293,6 +295,14 @@ def moe_layer(args: LayerArgs, out, ws, stream=None, stream2=None):
     rc = load().moe_layer(ctypes.byref(args), _ptr(out, torch.float32, "out"), _ptr(ws, None, "ws"),
                           ws.numel() * ws.element_size(), _stream(stream), s2)
     _check(rc, "moe_layer")
+
+
+def moe_selftest_bounded_wait(which: int, limit_us: int, ws, stream=None):
+    """Run a wait that nothing signals (0: mbarrier, 1: look-back flag); the
+    kernel must give up after limit_us and flag a timeout in ws."""
+    rc = load().moe_selftest_bounded_wait(which, limit_us, _ptr(ws, None, "ws"),
+                                          ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "moe_selftest_bounded_wait")
 
 
 def moe_check_error(ws, stream=None) -> tuple[int, int]:

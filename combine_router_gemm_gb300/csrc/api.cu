@@ -370,6 +370,18 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     return rc;
 }
 
+int moe_selftest_bounded_wait(int which, uint32_t limit_us, void* ws, size_t ws_bytes,
+                              void* stream) {
+    if ((which != 0 && which != 1) || limit_us < 1 || limit_us > 1000000) return MOE_ERR_INVALID_ARG;
+    if (!ws || !moe_host::aligned16(ws) || ws_bytes < ERR_BYTES + 256) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, ERR_BYTES + 256, s) != cudaSuccess) return MOE_ERR_CUDA;
+    uint32_t* err = static_cast<uint32_t*>(ws);
+    const uint64_t ns = 1000ull * limit_us;
+    if (which == 0) return moe_tc::mbar_probe(ns, err, s);
+    return moe_launch::lookback_probe(static_cast<char*>(ws) + ERR_BYTES, ns, err, s);
+}
+
 int moe_check_error(void* ws, void* stream, uint32_t* detail) {
     if (!ws) return MOE_ERR_INVALID_ARG;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;

@@ -74,6 +74,7 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
                      cudaStream_t s, cudaEvent_t between = nullptr,
                      const SharedExpert* sh = nullptr);
 size_t router_ws_bytes(int E, int d);
+int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s);
 int router_bf16(const void* x, const float* w_router, int T, int d, int E, int sigmoid,
                 float* scores, void* ws, uint32_t* err, cudaStream_t s);
 }  // namespace moe_tc
@@ -85,6 +86,7 @@ int router_gemm(const void* x, int dtype, const float* w_router, int T, int d, i
 int topk(const float* scores, const float* bias, int T, const moe_route_cfg* cfg, int32_t* idx,
          float* w, cudaStream_t s);
 size_t dispatch_ws_bytes(int T, int k, int E);
+int lookback_probe(void* flags_zeroed, uint64_t limit_ns, uint32_t* err, cudaStream_t s);
 int dispatch(const int32_t* idx, const void* x, int dtype, int T, int d, int k, int E, int32_t* counts,
              int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_token, void* x_perm, void* ws,
              uint32_t* err, cudaStream_t s);

@@ -70,6 +70,29 @@ __device__ __forceinline__ void st_release(int* p, int v) {
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Walk back from block b-1 until a block whose inclusive prefix is published
+// (flag 2), passing blocks that published only their aggregate (flag 1).
+// Returns that block (-1: none before b), or -2 if a predecessor published
+// nothing within limit_ns.
+__device__ int lookback_walk(const int* flags, int b, uint64_t limit_ns) {
+    int p = b - 1;
+    const uint64_t t0 = moe::globaltimer_ns();
+    while (p >= 0) {
+        const int f = ld_acquire(flags + p);
+        if (f == 2) return p;
+        if (f == 1) { --p; continue; }
+        if (moe::globaltimer_ns() - t0 > limit_ns) return -2;
+    }
+    return -1;
+}
+
+// Self-test of the bounded look-back wait: block 1 waits on block 0's flag,
+// which nothing sets; the wait must give up and report a timeout.
+__global__ void lookback_probe_kernel(const int* flags, uint64_t limit_ns, uint32_t* err) {
+    if (threadIdx.x == 0 && lookback_walk(flags, 1, limit_ns) == -2)
+        moe::raise_error(err, moe::ERR_TIMEOUT_SCAN);
+}
+
 __global__ void __launch_bounds__(DISP_THREADS) dispatch_count_kernel(
     const int32_t* __restrict__ idx, int S, int E, DispatchWs st, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, uint32_t* err) {
@@ -142,18 +165,12 @@ __global__ void __launch_bounds__(DISP_THREADS) dispatch_count_kernel(
         __syncthreads();
         if (tid == 0) {
             st_release(st.flags + b, 1);
-            // walk back until a block with its inclusive prefix published
-            int p = b - 1, stop = -1;
-            const uint64_t t0 = moe::globaltimer_ns();
-            while (p >= 0) {
-                const int f = ld_acquire(st.flags + p);
-                if (f == 2) { stop = p; break; }
-                if (f == 1) { --p; continue; }
-                if (moe::globaltimer_ns() - t0 > moe::WAIT_LIMIT_NS) {
-                    moe::raise_error(err, moe::ERR_TIMEOUT_SCAN);
-                    s_abort = 1;
-                    break;
-                }
+            // block 0 always publishes its inclusive prefix, so a walk that
+            // does not time out ends at some block >= 0
+            const int stop = lookback_walk(st.flags, b, moe::WAIT_LIMIT_NS);
+            if (stop < 0) {
+                moe::raise_error(err, moe::ERR_TIMEOUT_SCAN);
+                s_abort = 1;
             }
             s_stop = stop;
         }
@@ -237,6 +254,11 @@ __global__ void __launch_bounds__(256) permute_kernel(
 }  // namespace
 
 namespace moe_launch {
+
+int lookback_probe(void* flags_zeroed, uint64_t limit_ns, uint32_t* err, cudaStream_t s) {
+    lookback_probe_kernel<<<1, 32, 0, s>>>(static_cast<const int*>(flags_zeroed), limit_ns, err);
+    return moe_host::launch_status();
+}
 
 size_t dispatch_ws_bytes(int T, int k, int E) { return ws_bytes(T * k, E); }
 

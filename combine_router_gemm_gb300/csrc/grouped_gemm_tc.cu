@@ -49,37 +49,65 @@ constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 1024;
 
 // MODE 0: gate/up + SwiGLU (W1 and W3 tiles into two accumulators)
-// MODE 1: down projection (one A tile, double-buffered accumulator)
-// MODE 2: router, fp32 weight split into three bf16 terms (hi, mid, lo)
-//         that all accumulate into one accumulator
+// MODE 1: down projection (one A tile)
+// MODE 2: router, fp32 weight split into three bf16 terms (hi, mid, lo), one
+//         accumulator per term (tensor-core accumulation truncates at every
+//         MMA, so the small terms must not share the large term's
+//         accumulator), summed in the epilogue
+// BN is the token tile (MMA N upper bound).  Stages fill ~200 KB of shared
+// memory; accumulators are double-buffered when tensor memory allows.
+constexpr int SMEM_BUDGET = 200 * 1024;
+
 template <int MODE>
-struct Cfg;
+struct ModeCfg;
+// PF: how many k-blocks ahead of its loads the producer asks L2 to fetch the
+// same weight tiles (0 = never), so that the weight stream can keep more bytes
+// in flight than the shared-memory stages hold.
+#ifndef MOE_BN_GATE_UP
+#define MOE_BN_GATE_UP 256
+#endif
+#ifndef MOE_BN_DOWN
+#define MOE_BN_DOWN 256
+#endif
+#ifndef MOE_PF_GATE_UP
+#define MOE_PF_GATE_UP 0
+#endif
+#ifndef MOE_PF_DOWN
+#define MOE_PF_DOWN 0
+#endif
 template <>
-struct Cfg<0> {
-    static constexpr int NUM_A = 2, STAGES = 3, ACC_STAGES = 1, BN = 256;
+struct ModeCfg<0> {
+    static constexpr int NUM_A = 2, PF = MOE_PF_GATE_UP;
     static constexpr bool SPLIT_ACC = true;  // one accumulator per A tile
 };
 template <>
-struct Cfg<1> {
-    static constexpr int NUM_A = 1, STAGES = 4, ACC_STAGES = 2, BN = 256;
+struct ModeCfg<1> {
+    static constexpr int NUM_A = 1, PF = MOE_PF_DOWN;
     static constexpr bool SPLIT_ACC = false;
 };
 template <>
-struct Cfg<2> {
-    static constexpr int NUM_A = 3, STAGES = 3, ACC_STAGES = 2, BN = 64;
-    static constexpr bool SPLIT_ACC = false;
+struct ModeCfg<2> {
+    static constexpr int NUM_A = 3, PF = 0;
+    static constexpr bool SPLIT_ACC = true;
 };
 
-template <int MODE>
-__host__ __device__ constexpr int stage_bytes() {
-    return Cfg<MODE>::NUM_A * A_TILE_BYTES + Cfg<MODE>::BN * BK * 2;
-}
+template <int MODE, int BN_>
+struct Cfg {
+    static constexpr int NUM_A = ModeCfg<MODE>::NUM_A, BN = BN_, PF = ModeCfg<MODE>::PF;
+    static constexpr bool SPLIT_ACC = ModeCfg<MODE>::SPLIT_ACC;
+    static constexpr int STAGE_BYTES = NUM_A * A_TILE_BYTES + BN * BK * 2;
+    static constexpr int STAGES = SMEM_BUDGET / STAGE_BYTES;
+    static constexpr int ACC_COLS = SPLIT_ACC ? NUM_A * BN : BN;  // TMEM columns per accumulator
+    static constexpr int ACC_STAGES = TMEM_COLS / ACC_COLS >= 2 ? 2 : 1;
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + sizeof(int) * (MAX_E + 2);
+    static_assert(STAGES >= 2 && ACC_COLS <= TMEM_COLS, "tile does not fit");
+};
 
-template <int MODE>
-__host__ __device__ constexpr size_t smem_bytes() {
-    // 1 KB alignment slack + stages + barriers/tmem slot + schedule table
-    return 1024 + (size_t)Cfg<MODE>::STAGES * stage_bytes<MODE>() + 256 + sizeof(int) * (MAX_E + 2);
-}
+// Tensor maps of one activation matrix with token boxes of 32, 64, 128 and
+// 256 rows (index = log2(rows / 32)).
+struct BMaps {
+    CUtensorMap m[4];
+};
 
 struct Params {
     const int32_t* offsets;  // [E+1], or NULL: one segment [0, rows)
@@ -153,6 +181,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// Ask L2 to fetch a tile (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -270,22 +306,21 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* mpre, const int* o
 
 // ---------------------------------------------------------------- the kernel
 
-template <int MODE>
+template <int MODE, int BN_>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a,
-                           const __grid_constant__ CUtensorMap tm_b,
+                           const __grid_constant__ BMaps tm_b,
                            const __grid_constant__ CUtensorMap tm_a2,
-                           const __grid_constant__ CUtensorMap tm_b2, const Params p) {
-    using C = Cfg<MODE>;
+                           const __grid_constant__ BMaps tm_b2, const Params p) {
+    using C = Cfg<MODE, BN_>;
     constexpr int STAGES = C::STAGES, NUM_A = C::NUM_A, ACC = C::ACC_STAGES, BN = C::BN;
-    constexpr int ACC_COLS = C::SPLIT_ACC ? NUM_A * BN : BN;  // TMEM columns per accumulator stage
-    static_assert(ACC * ACC_COLS <= TMEM_COLS, "accumulators exceed tensor memory");
+    constexpr int ACC_COLS = C::ACC_COLS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* tiles = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)STAGES * stage_bytes<MODE>());
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)STAGES * C::STAGE_BYTES);
     uint64_t* full_bar = bars;                  // [STAGES]
     uint64_t* empty_bar = bars + STAGES;        // [STAGES]
     uint64_t* tfull_bar = bars + 2 * STAGES;    // [ACC]
@@ -294,7 +329,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* total_units = reinterpret_cast<int*>(tmem_slot + 2);
-    int* mpre = reinterpret_cast<int*>(smem + (size_t)STAGES * stage_bytes<MODE>() + 256);
+    int* mpre = reinterpret_cast<int*>(smem + (size_t)STAGES * C::STAGE_BYTES + 256);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // ---- schedule: token tiles per expert and their prefix (warp 0) -------
@@ -347,10 +382,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(smem_u32(drain_bar), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tm_a);
-        tma_prefetch_desc(&tm_b);
+        for (int i = 0; i < 4; ++i) tma_prefetch_desc(&tm_b.m[i]);
         if (p.rows2 > 0) {
             tma_prefetch_desc(&tm_a2);
-            tma_prefetch_desc(&tm_b2);
+            for (int i = 0; i < 4; ++i) tma_prefetch_desc(&tm_b2.m[i]);
         }
     }
     if (warp == 1) {
@@ -382,10 +417,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             long issued = 0;
+            // L2 prefetch cursor: walks the same (unit, k-block) sequence as
+            // the loads, C::PF k-blocks ahead of them
+            int pf_u = blockIdx.x, pf_kb = 0;
+            Unit pf_t{};
+            if (pf_u < U) pf_t = decode_unit<BN>(pf_u, mpre, offs, E, n_tiles, U, U2, p.rows2);
+            auto prefetch_next = [&]() {
+                if (C::PF == 0 || pf_u >= U) return;
+                const CUtensorMap* ma = pf_t.second ? &tm_a2 : &tm_a;
+                const int a_row = (pf_t.second ? 0 : pf_t.e * p.a_rows) + pf_t.n0;
+                const int kx = pf_kb * BK;
+#pragma unroll
+                for (int a = 0; a < NUM_A; ++a) tma_prefetch_l2(ma, kx, a_row + a * p.a_step);
+                if (++pf_kb == num_kb) {
+                    pf_kb = 0;
+                    pf_u += gridDim.x;
+                    if (pf_u < U) pf_t = decode_unit<BN>(pf_u, mpre, offs, E, n_tiles, U, U2, p.rows2);
+                }
+            };
+            for (int i = 0; i < C::PF; ++i) prefetch_next();
             for (int u = blockIdx.x; u < U && !*abort_flag; u += gridDim.x) {
                 const Unit t = decode_unit<BN>(u, mpre, offs, E, n_tiles, U, U2, p.rows2);
                 const CUtensorMap* ma = t.second ? &tm_a2 : &tm_a;
-                const CUtensorMap* mb = t.second ? &tm_b2 : &tm_b;
+                const CUtensorMap* mb = t.second ? tm_b2.m : tm_b.m;
                 const int nbox = (t.n_tok + B_BOX - 1) / B_BOX;
                 const uint32_t bytes = NUM_A * A_TILE_BYTES + nbox * B_BOX_BYTES;
                 const int a_row = (t.second ? 0 : t.e * p.a_rows) + t.n0;
@@ -396,17 +450,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t* st = tiles + (size_t)stage * stage_bytes<MODE>();
+                    uint8_t* st = tiles + (size_t)stage * C::STAGE_BYTES;
                     const uint32_t fb = smem_u32(&full_bar[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
                     const int kx = kb * BK;
 #pragma unroll
                     for (int a = 0; a < NUM_A; ++a)
                         tma_load_2d(smem_u32(st + a * A_TILE_BYTES), ma, fb, kx, a_row + a * p.a_step);
+                    // the token rows in at most four boxes of 256/128/64/32 rows
                     uint8_t* bdst = st + NUM_A * A_TILE_BYTES;
-                    for (int j = 0; j < nbox; ++j)
-                        tma_load_2d(smem_u32(bdst + j * B_BOX_BYTES), mb, fb, kx,
-                                    t.m_start + j * B_BOX);
+                    int row = 0;
+#pragma unroll
+                    for (int lv = 3; lv >= 0; --lv) {
+                        const int h = B_BOX << lv;
+                        if (h <= BN && (nbox * B_BOX - row) >= h) {
+                            tma_load_2d(smem_u32(bdst + row * BK * 2), mb + lv, fb, kx,
+                                        t.m_start + row);
+                            row += h;
+                        }
+                    }
+                    prefetch_next();
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -449,7 +512,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t st = smem_u32(tiles + (size_t)stage * stage_bytes<MODE>());
+                    const uint32_t st = smem_u32(tiles + (size_t)stage * C::STAGE_BYTES);
                     const uint32_t bsm = st + NUM_A * A_TILE_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
@@ -514,18 +577,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             H[(size_t)(t.m_start + tok) * p.N_out + n] = __float2bfloat16_rn(h);
                         }
                     }
-                } else {
+                } else if (MODE == 2) {
+                    uint32_t mid[32], lo[32];
+                    tmem_ld32(tbase + BN + c0, mid);
+                    tmem_ld32(tbase + 2 * BN + c0, lo);
                     tmem_wait_ld();
                     float* Y = static_cast<float*>(out);
-                    const bool sig = MODE == 2 && (p.flags & 1);
+                    const bool sig = p.flags & 1;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int tok = c0 + j;
                         if (n_ok && tok < t.n_tok) {
-                            float v = __uint_as_float(g[j]);
+                            float v = __uint_as_float(g[j]) +
+                                      (__uint_as_float(mid[j]) + __uint_as_float(lo[j]));
                             if (sig) v = 1.0f / (1.0f + expf(-v));
                             Y[(size_t)(t.m_start + tok) * p.N_out + n] = v;
                         }
+                    }
+                } else {
+                    tmem_wait_ld();
+                    float* Y = static_cast<float*>(out);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int tok = c0 + j;
+                        if (n_ok && tok < t.n_tok)
+                            Y[(size_t)(t.m_start + tok) * p.N_out + n] = __uint_as_float(g[j]);
                     }
                 }
             }
@@ -544,6 +620,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                      "r"(TMEM_COLS)
                      : "memory");
     }
+}
+
+// Self-test of the bounded pipeline wait: an mbarrier that nothing arrives
+// on; the wait must give up and report a timeout.
+__global__ void mbar_probe_kernel(uint64_t limit_ns, uint32_t* err) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, err, limit_ns);
 }
 
 // Router weight split: w = hi + mid + lo with each term the bf16 rounding of
@@ -594,19 +684,25 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
     return r == CUDA_SUCCESS;
 }
 
-template <int MODE>
-int launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& a2,
-           const CUtensorMap& b2, const Params& p, cudaStream_t s) {
+bool make_bmaps(BMaps* m, const void* base, uint64_t rows, uint64_t cols) {
+    for (int i = 0; i < 4; ++i)
+        if (!make_map(&m->m[i], base, rows, cols, (uint32_t)(B_BOX << i))) return false;
+    return true;
+}
+
+template <int MODE, int BN>
+int launch(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, const BMaps& b2,
+           const Params& p, cudaStream_t s) {
     static bool attr_done = false;
-    const size_t smem = smem_bytes<MODE>();
+    const size_t smem = Cfg<MODE, BN>::SMEM;
     if (!attr_done) {
-        if (cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE>,
+        if (cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, BN>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
             return MOE_ERR_CUDA;
         attr_done = true;
     }
-    grouped_gemm_tc_kernel<MODE><<<moe_host::num_sms(), NUM_THREADS, smem, s>>>(a, b, a2, b2, p);
+    grouped_gemm_tc_kernel<MODE, BN><<<moe_host::num_sms(), NUM_THREADS, smem, s>>>(a, b, a2, b2, p);
     return moe_host::launch_status();
 }
 
@@ -621,26 +717,33 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
                      const void* w13, const void* w2, float* y, void* h, uint32_t* err,
                      cudaStream_t s, cudaEvent_t between, const SharedExpert* sh) {
     if (E > MAX_E) return MOE_ERR_UNSUPPORTED;
-    CUtensorMap a1, b1, a2, b2, a1s, b1s, a2s, b2s;
-    if (!make_map(&a1, w13, (uint64_t)E * 2 * I, d, BM) ||
-        !make_map(&b1, x_perm, rows, d, B_BOX) ||
-        !make_map(&a2, w2, (uint64_t)E * d, I, BM) ||
-        !make_map(&b2, h, rows, I, B_BOX))
+    CUtensorMap a1, a2, a1s, a2s;
+    BMaps b1, b2, b1s, b2s;
+    if (!make_map(&a1, w13, (uint64_t)E * 2 * I, d, BM) || !make_bmaps(&b1, x_perm, rows, d) ||
+        !make_map(&a2, w2, (uint64_t)E * d, I, BM) || !make_bmaps(&b2, h, rows, I))
         return MOE_ERR_CUDA;
     const bool two = sh != nullptr && sh->T > 0;
     if (two) {
-        if (!make_map(&a1s, sh->w13, 2ull * I, d, BM) || !make_map(&b1s, sh->x, sh->T, d, B_BOX) ||
-            !make_map(&a2s, sh->w2, (uint64_t)d, I, BM) || !make_map(&b2s, sh->h, sh->T, I, B_BOX))
+        if (!make_map(&a1s, sh->w13, 2ull * I, d, BM) || !make_bmaps(&b1s, sh->x, sh->T, d) ||
+            !make_map(&a2s, sh->w2, (uint64_t)d, I, BM) || !make_bmaps(&b2s, sh->h, sh->T, I))
             return MOE_ERR_CUDA;
     } else {
         a1s = a1; b1s = b1; a2s = a2; b2s = b2;
     }
     Params p1{offsets, E, rows, d, I, 2 * I, I, h, err, 0, two ? sh->T : 0, two ? sh->h : nullptr};
-    int rc = launch<0>(a1, b1, a1s, b1s, p1, s);
+    Params p2{offsets, E, rows, I, d, d, 0, y, err, 0, two ? sh->T : 0, two ? sh->y : nullptr};
+    // Token tile 256: a weight tile enters one SM once per 256 tokens of its
+    // expert (smaller tiles make experts of 129-256 rows pull every weight
+    // tile into two SMs, which costs L2 bandwidth the weight stream needs).
+    int rc = launch<0, MOE_BN_GATE_UP>(a1, b1, a1s, b1s, p1, s);
     if (rc != MOE_OK) return rc;
     if (between && cudaEventRecord(between, s) != cudaSuccess) return MOE_ERR_CUDA;
-    Params p2{offsets, E, rows, I, d, d, 0, y, err, 0, two ? sh->T : 0, two ? sh->y : nullptr};
-    return launch<1>(a2, b2, a2s, b2s, p2, s);
+    return launch<1, MOE_BN_DOWN>(a2, b2, a2s, b2s, p2, s);
+}
+
+int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s) {
+    mbar_probe_kernel<<<1, 32, 0, s>>>(limit_ns, err);
+    return moe_host::launch_status();
 }
 
 size_t router_ws_bytes(int E, int d) { return (size_t)3 * E * d * 2; }
@@ -655,10 +758,11 @@ int router_bf16(const void* x, const float* w_router, int T, int d, int E, int s
     split_weight_kernel<<<blocks, 256, 0, s>>>(w_router, n, wsplit);
     int rc = moe_host::launch_status();
     if (rc != MOE_OK) return rc;
-    CUtensorMap a, b;
-    if (!make_map(&a, wsplit, 3ull * E, d, BM) || !make_map(&b, x, T, d, B_BOX)) return MOE_ERR_CUDA;
+    CUtensorMap a;
+    BMaps b;
+    if (!make_map(&a, wsplit, 3ull * E, d, BM) || !make_bmaps(&b, x, T, d)) return MOE_ERR_CUDA;
     Params p{nullptr, 1, T, d, E, 0, E, scores, err, sigmoid ? 1 : 0, 0, nullptr};
-    return launch<2>(a, b, a, b, p, s);
+    return launch<2, 64>(a, b, a, b, p, s);
 }
 
 }  // namespace moe_tc

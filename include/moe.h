@@ -238,6 +238,17 @@ int moe_dispatch_noalloc(const int32_t* topk_idx, const void* x, int dtype, int 
  * (host pointer, may be NULL) receives the raw error word. */
 int moe_check_error(void* ws, void* stream, uint32_t* detail);
 
+/* Self-test of the bounded device waits (failure detection without a fault).
+ * Launches one tiny kernel that waits on something nothing will ever signal:
+ * which = 0: an mbarrier, as in the grouped-GEMM pipeline; which = 1: a
+ * predecessor's look-back flag, as in the dispatch scan.  The wait gives up
+ * after limit_us microseconds (1..1000000) and sets the error word of `ws`
+ * (>= 512 bytes, any contents); moe_check_error(ws, ...) then returns
+ * MOE_ERR_TIMEOUT.  The kernels of the layer use the same waits with a
+ * one-second limit. */
+int moe_selftest_bounded_wait(int which, uint32_t limit_us, void* ws, size_t ws_bytes,
+                              void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -13,6 +13,14 @@ F32_REL_FRO = 1e-5
 GATE_RTOL = 4e-6
 
 
+def tc_router_atol(d: int, magnitude: float = 4.0) -> float:
+    """Error bound of router scores from the tensor cores: the fp32 accumulator
+    is truncated once per MMA (16 products), so over d/16 MMAs with partial
+    sums up to `magnitude` the error is at most (d/16) * 2^-23 * magnitude
+    (the split-weight terms have accumulators of their own, far smaller)."""
+    return (d / 16) * 2.0 ** -23 * magnitude
+
+
 def np_(t):
     return inputs.to_numpy(t)
 
@@ -35,11 +43,13 @@ def assert_bf16_close(got, ref, what=""):
 
 
 def near_tie_tokens(scores: np.ndarray, bias, k: int, n_group: int = 1, topk_group: int = 1,
-                    rel: float = 1e-5):
-    """Tokens whose selection is decided by a margin smaller than ``rel``: the
-    k-th vs (k+1)-th eligible key, or (group-limited routing) the topk_group-th
-    vs next group score.  Between two fp32 score tensors that differ only by
-    rounding, the choice may legitimately flip on exactly these tokens."""
+                    rel: float = 1e-5, abs_margin: float = 0.0):
+    """Tokens whose selection is decided by a margin smaller than ``rel``
+    (relative) plus twice ``abs_margin`` (the score error bound of the router
+    that made the other tensor): the k-th vs (k+1)-th eligible key, or
+    (group-limited routing) the topk_group-th vs next group score.  Between two
+    score tensors that differ only by rounding, the choice may legitimately
+    flip on exactly these tokens."""
     key = scores.astype(np.float64) + (0 if bias is None else bias.astype(np.float64))
     T, E = key.shape
     amb = np.zeros(T, bool)
@@ -50,7 +60,7 @@ def near_tie_tokens(scores: np.ndarray, bias, k: int, n_group: int = 1, topk_gro
         g_sorted = np.take_along_axis(top2, order, 1)
         if topk_group < n_group:
             gap = np.abs(g_sorted[:, topk_group - 1] - g_sorted[:, topk_group])
-            amb |= gap <= rel * np.maximum(1.0, np.abs(g_sorted[:, topk_group - 1]))
+            amb |= gap <= rel * np.maximum(1.0, np.abs(g_sorted[:, topk_group - 1])) + 4 * abs_margin
         keep = np.zeros((T, n_group), bool)
         np.put_along_axis(keep, order[:, :topk_group], True, 1)
         key = np.where(np.repeat(keep, gs, axis=1), key, -np.inf)
@@ -58,7 +68,7 @@ def near_tie_tokens(scores: np.ndarray, bias, k: int, n_group: int = 1, topk_gro
     if srt.shape[1] > k and np.isfinite(srt[:, k]).any():
         nxt = srt[:, k]
         gap = np.where(np.isfinite(nxt), np.abs(srt[:, k - 1] - nxt), np.inf)
-        amb |= gap <= rel * np.maximum(1.0, np.abs(srt[:, k - 1]))
+        amb |= gap <= rel * np.maximum(1.0, np.abs(srt[:, k - 1])) + 2 * abs_margin
     return amb
 
 

@@ -13,7 +13,8 @@ import torch
 
 from combine_router_gemm_gb300 import binding as B
 from combine_router_gemm_gb300 import inputs
-from helpers import F32_REL_FRO, assert_bf16_close, cuda_f32, cuda_i32, near_tie_tokens, np_, rel_fro
+from helpers import (F32_REL_FRO, assert_bf16_close, cuda_f32, cuda_i32, near_tie_tokens, np_,
+                     rel_fro, tc_router_atol)
 
 pytestmark = pytest.mark.gpu
 
@@ -84,7 +85,8 @@ def test_layer_small_bf16_all_tokens(oracle, cfg, overlap):
     out, idx, w, scores, offs = run_layer(cfg, inp, overlap)
     sc, ridx, rw, rout = oracle_tokens(oracle, cfg, inp, torch.arange(cfg.T, device="cuda"))
     same = (np_(idx) == ridx).all(1)
-    amb = near_tie_tokens(sc, np_(inp["bias"]), cfg.k, cfg.n_group, cfg.topk_group)
+    amb = near_tie_tokens(sc, np_(inp["bias"]), cfg.k, cfg.n_group, cfg.topk_group,
+                          abs_margin=tc_router_atol(cfg.d))
     assert (same | amb).all()
     assert_bf16_close(np_(out)[same], rout[same], cfg.name)
 
@@ -111,7 +113,8 @@ def test_layer_full_size_sampled(oracle, name):
     sc, ridx, rw, rout = oracle_tokens(oracle, cfg, inp, tok.cuda())
     gidx = np_(idx[tok.cuda()])
     same = (gidx == ridx).all(1)
-    amb = near_tie_tokens(sc, np_(inp["bias"]), cfg.k, cfg.n_group, cfg.topk_group)
+    amb = near_tie_tokens(sc, np_(inp["bias"]), cfg.k, cfg.n_group, cfg.topk_group,
+                          abs_margin=tc_router_atol(cfg.d))
     assert (same | amb).all()
     assert_bf16_close(np_(out[tok.cuda()])[same], rout[same], name)
     del inp, out
