@@ -63,12 +63,6 @@ struct ModeCfg;
 // PF: how many k-blocks ahead of its loads the producer asks L2 to fetch the
 // same weight tiles (0 = never), so that the weight stream can keep more bytes
 // in flight than the shared-memory stages hold.
-#ifndef MOE_BN_GATE_UP
-#define MOE_BN_GATE_UP 256
-#endif
-#ifndef MOE_BN_DOWN
-#define MOE_BN_DOWN 256
-#endif
 #ifndef MOE_PF_GATE_UP
 #define MOE_PF_GATE_UP 0
 #endif
@@ -732,13 +726,23 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     }
     Params p1{offsets, E, rows, d, I, 2 * I, I, h, err, 0, two ? sh->T : 0, two ? sh->h : nullptr};
     Params p2{offsets, E, rows, I, d, d, 0, y, err, 0, two ? sh->T : 0, two ? sh->y : nullptr};
-    // Token tile 256: a weight tile enters one SM once per 256 tokens of its
-    // expert (smaller tiles make experts of 129-256 rows pull every weight
-    // tile into two SMs, which costs L2 bandwidth the weight stream needs).
-    int rc = launch<0, MOE_BN_GATE_UP>(a1, b1, a1s, b1s, p1, s);
+    // Token tile per launch, from the average rows per expert (the host does
+    // not see the device-side offsets).  A 128-row tile leaves room for one
+    // more shared-memory stage, so more weight bytes in flight (and, for
+    // gate/up, a double-buffered accumulator); a 256-row tile brings each
+    // weight tile into one SM once for experts of 129-256 rows and halves
+    // the shared-memory traffic per MMA when the GEMM is compute-bound.
+    //   gate/up: 128 below 384 rows per expert (measured: DeepSeek-V3 prefill
+    //            2.67 ms vs 2.85 ms), else 256;
+    //   down:    128 only below 32 rows per expert (decode), else 256
+    //            (prefill: 1.57 ms vs 2.01 ms).
+    const long long avg_x = (long long)rows;  // compare rows with k * E
+    const bool gu_wide = avg_x >= 384LL * E;
+    const bool dn_wide = avg_x >= 32LL * E;
+    int rc = gu_wide ? launch<0, 256>(a1, b1, a1s, b1s, p1, s) : launch<0, 128>(a1, b1, a1s, b1s, p1, s);
     if (rc != MOE_OK) return rc;
     if (between && cudaEventRecord(between, s) != cudaSuccess) return MOE_ERR_CUDA;
-    return launch<1, MOE_BN_DOWN>(a2, b2, a2s, b2s, p2, s);
+    return dn_wide ? launch<1, 256>(a2, b2, a2s, b2s, p2, s) : launch<1, 128>(a2, b2, a2s, b2s, p2, s);
 }
 
 int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s) {
