@@ -65,6 +65,22 @@ def peaks():
     return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
+def max_over_ranks(x: float, device="cuda") -> float:
+    """The largest x over all ranks (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(tokens_per_step: int, steps: int, world: int, seconds: float) -> float:
+    """Tokens/s of the whole job: every rank's tokens over the slowest rank's time."""
+    return tokens_per_step * steps * world / seconds
+
+
 def env_rank():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
             int(os.environ.get("WORLD_SIZE", "1")))
@@ -283,12 +299,8 @@ def run_ours(args, cfg):
     step_ms = [e[0].elapsed_time(e[-1]) for e in evs]
     stage_ms = [statistics.fmean(e[i].elapsed_time(e[i + 1]) for e in evs)
                 for i in range(B.LAYER_EVENTS - 1)]
-    total_s = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
-    value = cfg.T * K * world / total_s
+    total_s = max_over_ranks(sum(step_ms) / 1e3)
+    value = whole_job_value(cfg.T, K, world, total_s)
 
     # ---- algorithmic work per stage (bytes / flops per launch)
     o = offs.cpu().numpy()
@@ -363,12 +375,9 @@ def run_ours(args, cfg):
             oh.copy_(out, non_blocking=True)
         ee_.record()
         torch.cuda.synchronize()
-        e_s = es_.elapsed_time(ee_) / 1e3
-        if world > 1:
-            t = torch.tensor([e_s], device="cuda", dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_s = float(t.item())
-        e2e = {"value": T * ne * world / e_s, "unit": UNIT, "h2d_bytes_per_step": T * d * x.element_size(),
+        e_s = max_over_ranks(es_.elapsed_time(ee_) / 1e3)
+        e2e = {"value": whole_job_value(T, ne, world, e_s), "unit": UNIT,
+               "h2d_bytes_per_step": T * d * x.element_size(),
                "d2h_bytes_per_step": T * d * 4, "steps": ne}
 
     cpu = None
