@@ -15,9 +15,10 @@
 //    N side walks tokens (16..256, rounded up to 16 per tile).  Small and
 //    ragged segments then cost N granularity 16 rather than a 128-row tile,
 //    and every weight tile of an expert is read once per 256 tokens.
-//  * One CTA per SM (persistent), 6 warps: warp 0 issues TMA loads, warp 1
-//    allocates tensor memory and issues tcgen05.mma from one thread, warps 2-5
-//    drain the accumulators (tcgen05.ld) and store.  Shared-memory stages are
+//  * One CTA per SM (persistent), 10 warps: warp 0 issues TMA loads, warp 1
+//    allocates tensor memory and issues tcgen05.mma from one thread, warps 2-9
+//    drain the accumulators (tcgen05.ld; two warps per 32-lane quarter) and
+//    store.  Shared-memory stages are
 //    handed over with mbarriers; the accumulator is handed over with a
 //    full/empty mbarrier pair (double-buffered in the down GEMM).
 //  * Operands are K-major bf16 tiles of 64 elements (128 B) per row, loaded by
@@ -44,7 +45,8 @@ constexpr int BK = 64;          // K per stage: one 128-byte swizzle atom row
 constexpr int B_BOX = 32;       // token rows per TMA box
 constexpr int A_TILE_BYTES = BM * BK * 2;      // 16 KB
 constexpr int B_BOX_BYTES = B_BOX * BK * 2;    // 4 KB
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_WARPS = 8;  // two per 32-lane quarter of tensor memory
+constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS);
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 1024;
 
@@ -76,8 +78,9 @@ struct ModeCfg<0> {
 };
 template <>
 struct ModeCfg<1> {
-    static constexpr int NUM_A = 1, PF = MOE_PF_DOWN;
-    static constexpr bool SPLIT_ACC = false;
+    // two 128-feature tiles (a_step = 128 rows apart) share each token tile
+    static constexpr int NUM_A = 2, PF = MOE_PF_DOWN;
+    static constexpr bool SPLIT_ACC = true;
 };
 template <>
 struct ModeCfg<2> {
@@ -92,6 +95,9 @@ struct Cfg {
     static constexpr int STAGE_BYTES = NUM_A * A_TILE_BYTES + BN * BK * 2;
     static constexpr int STAGES = SMEM_BUDGET / STAGE_BYTES;
     static constexpr int ACC_COLS = SPLIT_ACC ? NUM_A * BN : BN;  // TMEM columns per accumulator
+    // output features per unit: the down projection's A tiles are distinct
+    // features; gate/up (W1, W3) and the router's weight terms share features
+    static constexpr int FEAT = MODE == 1 ? NUM_A * BM : BM;
     static constexpr int ACC_STAGES = TMEM_COLS / ACC_COLS >= 2 ? 2 : 1;
     static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + sizeof(int) * (MAX_E + 2);
     static_assert(STAGES >= 2 && ACC_COLS <= TMEM_COLS, "tile does not fit");
@@ -262,7 +268,7 @@ struct Unit {
 // feature tile is the major index and the token tile the minor one.  Units of
 // the second problem (U2 of them) are spread evenly through the sequence: with
 // period P = U / U2, position j*P holds second-problem unit j.
-template <int BN>
+template <int BN, int FEAT>
 __device__ __forceinline__ Unit decode_unit(int u, const int* mpre, const int* offs, int E,
                                             int n_tiles, int U, int U2, int rows2) {
     Unit r;
@@ -276,7 +282,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* mpre, const int* o
             r.second = true;
             r.m_start = mtile * BN;
             r.n_tok = min(BN, rows2 - r.m_start);
-            r.n0 = nt * BM;
+            r.n0 = nt * FEAT;
             return r;
         }
         u -= min(U2, j + 1);
@@ -294,7 +300,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* mpre, const int* o
     r.second = false;
     r.m_start = offs[e] + mtile * BN;
     r.n_tok = min(BN, offs[e + 1] - r.m_start);
-    r.n0 = nt * BM;
+    r.n0 = nt * FEAT;
     return r;
 }
 
@@ -328,7 +334,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     // ---- schedule: token tiles per expert and their prefix (warp 0) -------
     const int E = p.E;
-    const int n_tiles = (p.N_out + BM - 1) / BM;
+    const int n_tiles = (p.N_out + C::FEAT - 1) / C::FEAT;
     const int U2 = p.rows2 > 0 ? ((p.rows2 + BN - 1) / BN) * n_tiles : 0;
     if (warp == 0) {
         // per-lane chunk of experts, then a warp scan of the chunk sums
@@ -371,7 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int a = 0; a < ACC; ++a) {
             mbar_init(smem_u32(&tfull_bar[a]), 1);
-            mbar_init(smem_u32(&tempty_bar[a]), 4);
+            mbar_init(smem_u32(&tempty_bar[a]), NUM_EPI_WARPS);
         }
         mbar_init(smem_u32(drain_bar), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -415,7 +421,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // the loads, C::PF k-blocks ahead of them
             int pf_u = blockIdx.x, pf_kb = 0;
             Unit pf_t{};
-            if (pf_u < U) pf_t = decode_unit<BN>(pf_u, mpre, offs, E, n_tiles, U, U2, p.rows2);
+            if (pf_u < U) pf_t = decode_unit<BN, C::FEAT>(pf_u, mpre, offs, E, n_tiles, U, U2, p.rows2);
             auto prefetch_next = [&]() {
                 if (C::PF == 0 || pf_u >= U) return;
                 const CUtensorMap* ma = pf_t.second ? &tm_a2 : &tm_a;
@@ -426,12 +432,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (++pf_kb == num_kb) {
                     pf_kb = 0;
                     pf_u += gridDim.x;
-                    if (pf_u < U) pf_t = decode_unit<BN>(pf_u, mpre, offs, E, n_tiles, U, U2, p.rows2);
+                    if (pf_u < U) pf_t = decode_unit<BN, C::FEAT>(pf_u, mpre, offs, E, n_tiles, U, U2, p.rows2);
                 }
             };
             for (int i = 0; i < C::PF; ++i) prefetch_next();
             for (int u = blockIdx.x; u < U && !*abort_flag; u += gridDim.x) {
-                const Unit t = decode_unit<BN>(u, mpre, offs, E, n_tiles, U, U2, p.rows2);
+                const Unit t = decode_unit<BN, C::FEAT>(u, mpre, offs, E, n_tiles, U, U2, p.rows2);
                 const CUtensorMap* ma = t.second ? &tm_a2 : &tm_a;
                 const CUtensorMap* mb = t.second ? tm_b2.m : tm_b.m;
                 const int nbox = (t.n_tok + B_BOX - 1) / B_BOX;
@@ -490,7 +496,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t acc_phase = 0;
             bool issued_any = false;
             for (int u = blockIdx.x; u < U && !*abort_flag; u += gridDim.x) {
-                const Unit t = decode_unit<BN>(u, mpre, offs, E, n_tiles, U, U2, p.rows2);
+                const Unit t = decode_unit<BN, C::FEAT>(u, mpre, offs, E, n_tiles, U, U2, p.rows2);
                 const int bn = (t.n_tok + 15) & ~15;
                 const uint32_t idesc = idesc_bf16(bn);
                 if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, abort_flag, p.err,
@@ -539,11 +545,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (U > 0 && warp >= 2) {
         // ================= epilogue: tensor memory -> global =================
-        const int q = warp & 3;  // this warp's quarter of the 128 TMEM lanes
+        // warps 2..9: quarter q = warp % 4 of the 128 TMEM lanes (hardware
+        // rule), the two warps of a quarter take alternate 32-token chunks
+        const int q = warp & 3;
+        const int sub = (warp - 2) >> 2;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < U; u += gridDim.x) {
-            const Unit t = decode_unit<BN>(u, mpre, offs, E, n_tiles, U, U2, p.rows2);
+            const Unit t = decode_unit<BN, C::FEAT>(u, mpre, offs, E, n_tiles, U, U2, p.rows2);
             if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.err,
                            moe::WAIT_LIMIT_NS))
                 break;
@@ -553,7 +562,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             void* out = t.second ? p.out2 : p.out;
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
-            for (int c0 = 0; c0 < t.n_tok; c0 += 32) {
+            for (int c0 = 32 * sub; c0 < t.n_tok; c0 += 64) {
                 uint32_t g[32];
                 tmem_ld32(tbase + c0, g);
                 if (MODE == 0) {
@@ -567,7 +576,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (n_ok && tok < t.n_tok) {
                             const float gv = __uint_as_float(g[j]);
                             const float uv = __uint_as_float(up[j]);
-                            const float h = gv / (1.0f + __expf(-gv)) * uv;
+                            // silu(g) * u; the fast divide's few-ulp error
+                            // vanishes in the bf16 rounding of h
+                            const float h = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
                             H[(size_t)(t.m_start + tok) * p.N_out + n] = __float2bfloat16_rn(h);
                         }
                     }
@@ -589,13 +600,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                 } else {
+                    uint32_t g2[32];
+                    tmem_ld32(tbase + BN + c0, g2);
                     tmem_wait_ld();
                     float* Y = static_cast<float*>(out);
+                    const int n2 = n + BM;  // the second feature tile
+                    const bool n2_ok = n2 < p.N_out;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int tok = c0 + j;
-                        if (n_ok && tok < t.n_tok)
-                            Y[(size_t)(t.m_start + tok) * p.N_out + n] = __uint_as_float(g[j]);
+                        if (tok < t.n_tok) {
+                            float* row = Y + (size_t)(t.m_start + tok) * p.N_out;
+                            if (n_ok) row[n] = __uint_as_float(g[j]);
+                            if (n2_ok) row[n2] = __uint_as_float(g2[j]);
+                        }
                     }
                 }
             }
@@ -725,7 +743,7 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
         a1s = a1; b1s = b1; a2s = a2; b2s = b2;
     }
     Params p1{offsets, E, rows, d, I, 2 * I, I, h, err, 0, two ? sh->T : 0, two ? sh->h : nullptr};
-    Params p2{offsets, E, rows, I, d, d, 0, y, err, 0, two ? sh->T : 0, two ? sh->y : nullptr};
+    Params p2{offsets, E, rows, I, d, d, BM, y, err, 0, two ? sh->T : 0, two ? sh->y : nullptr};
     // Token tile per launch, from the average rows per expert (the host does
     // not see the device-side offsets).  A 128-row tile leaves room for one
     // more shared-memory stage, so more weight bytes in flight (and, for
