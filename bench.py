@@ -45,14 +45,14 @@ def launches_per_step(cfg) -> int:
     return n
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the routed
-# gate/up GEMM per launch, from one ncu capture of this kernel source on the
-# 32-expert workload, scaled x8 (experts and tokens) to the 256-expert layer
+# (+ shared) gate/up GEMM per launch, from one ncu capture of this kernel
+# source on the 32-expert workload; at the 256-expert layer the routed part is
+# scaled x8 (experts and tokens) and the shared expert's weights are not
 # (profiles/grouped_gemm_tc_dsv3_prefill_e32.md).  Reported as null once the
-# kernel source no longer matches the captured one.  (That capture ran the
-# routed experts alone; the shared expert now shares the launch.)
-TRAFFIC = {"source_sha256": "249a4017ed745cdd01a8c3cd64389efc3c0731e27db542ac4c058850f7b3d0d8",
-           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.961467e9,
-                                            "dsv3_prefill": 8 * 1.961467e9}}
+# kernel source no longer matches the captured one.
+TRAFFIC = {"source_sha256": "84a03aedeee0d4888088de0ab968c7d76ed81b9e03f4e9b0b5f919f25a85a216",
+           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 2.086918e9,
+                                            "dsv3_prefill": 8 * (2.086918e9 - 0.0587e9) + 0.0587e9}}
 
 
 def peaks():

@@ -65,6 +65,14 @@ struct ModeCfg;
 // PF: how many k-blocks ahead of its loads the producer asks L2 to fetch the
 // same weight tiles (0 = never), so that the weight stream can keep more bytes
 // in flight than the shared-memory stages hold.
+// rows per expert from which the gate/up and down launches use 256-row token
+// tiles (below: 128)
+#ifndef MOE_GU_WIDE_ROWS
+#define MOE_GU_WIDE_ROWS 384
+#endif
+#ifndef MOE_DN_WIDE_ROWS
+#define MOE_DN_WIDE_ROWS 32
+#endif
 #ifndef MOE_PF_GATE_UP
 #define MOE_PF_GATE_UP 0
 #endif
@@ -754,9 +762,8 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     //            2.67 ms vs 2.85 ms), else 256;
     //   down:    128 only below 32 rows per expert (decode), else 256
     //            (prefill: 1.57 ms vs 2.01 ms).
-    const long long avg_x = (long long)rows;  // compare rows with k * E
-    const bool gu_wide = avg_x >= 384LL * E;
-    const bool dn_wide = avg_x >= 32LL * E;
+    const bool gu_wide = (long long)rows >= (long long)MOE_GU_WIDE_ROWS * E;
+    const bool dn_wide = (long long)rows >= (long long)MOE_DN_WIDE_ROWS * E;
     int rc = gu_wide ? launch<0, 256>(a1, b1, a1s, b1s, p1, s) : launch<0, 128>(a1, b1, a1s, b1s, p1, s);
     if (rc != MOE_OK) return rc;
     if (between && cudaEventRecord(between, s) != cudaSuccess) return MOE_ERR_CUDA;
