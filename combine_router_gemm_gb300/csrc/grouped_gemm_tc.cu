@@ -62,9 +62,6 @@ constexpr int SMEM_BUDGET = 200 * 1024;
 
 template <int MODE>
 struct ModeCfg;
-// PF: how many k-blocks ahead of its loads the producer asks L2 to fetch the
-// same weight tiles (0 = never), so that the weight stream can keep more bytes
-// in flight than the shared-memory stages hold.
 // rows per expert from which the gate/up and down launches use 256-row token
 // tiles (below: 128)
 #ifndef MOE_GU_WIDE_ROWS
@@ -73,32 +70,26 @@ struct ModeCfg;
 #ifndef MOE_DN_WIDE_ROWS
 #define MOE_DN_WIDE_ROWS 32
 #endif
-#ifndef MOE_PF_GATE_UP
-#define MOE_PF_GATE_UP 0
-#endif
-#ifndef MOE_PF_DOWN
-#define MOE_PF_DOWN 0
-#endif
 template <>
 struct ModeCfg<0> {
-    static constexpr int NUM_A = 2, PF = MOE_PF_GATE_UP;
+    static constexpr int NUM_A = 2;
     static constexpr bool SPLIT_ACC = true;  // one accumulator per A tile
 };
 template <>
 struct ModeCfg<1> {
     // two 128-feature tiles (a_step = 128 rows apart) share each token tile
-    static constexpr int NUM_A = 2, PF = MOE_PF_DOWN;
+    static constexpr int NUM_A = 2;
     static constexpr bool SPLIT_ACC = true;
 };
 template <>
 struct ModeCfg<2> {
-    static constexpr int NUM_A = 3, PF = 0;
+    static constexpr int NUM_A = 3;
     static constexpr bool SPLIT_ACC = true;
 };
 
 template <int MODE, int BN_>
 struct Cfg {
-    static constexpr int NUM_A = ModeCfg<MODE>::NUM_A, BN = BN_, PF = ModeCfg<MODE>::PF;
+    static constexpr int NUM_A = ModeCfg<MODE>::NUM_A, BN = BN_;
     static constexpr bool SPLIT_ACC = ModeCfg<MODE>::SPLIT_ACC;
     static constexpr int STAGE_BYTES = NUM_A * A_TILE_BYTES + BN * BK * 2;
     static constexpr int STAGES = SMEM_BUDGET / STAGE_BYTES;
@@ -107,6 +98,7 @@ struct Cfg {
     // features; gate/up (W1, W3) and the router's weight terms share features
     static constexpr int FEAT = MODE == 1 ? NUM_A * BM : BM;
     static constexpr int ACC_STAGES = TMEM_COLS / ACC_COLS >= 2 ? 2 : 1;
+    // + barriers/tmem slot + schedule table
     static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + sizeof(int) * (MAX_E + 2);
     static_assert(STAGES >= 2 && ACC_COLS <= TMEM_COLS, "tile does not fit");
 };
@@ -189,14 +181,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
-}
-
-// Ask L2 to fetch a tile (no shared memory, no completion to wait for).
-__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y)
-                 : "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -420,30 +404,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int num_kb = (p.K + BK - 1) / BK;
 
     if (U > 0 && warp == 0) {
-        // ================= TMA producer =================
+        // ================= TMA producer (one thread) =================
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             long issued = 0;
-            // L2 prefetch cursor: walks the same (unit, k-block) sequence as
-            // the loads, C::PF k-blocks ahead of them
-            int pf_u = blockIdx.x, pf_kb = 0;
-            Unit pf_t{};
-            if (pf_u < U) pf_t = decode_unit<BN, C::FEAT>(pf_u, mpre, offs, E, n_tiles, U, U2, p.rows2);
-            auto prefetch_next = [&]() {
-                if (C::PF == 0 || pf_u >= U) return;
-                const CUtensorMap* ma = pf_t.second ? &tm_a2 : &tm_a;
-                const int a_row = (pf_t.second ? 0 : pf_t.e * p.a_rows) + pf_t.n0;
-                const int kx = pf_kb * BK;
-#pragma unroll
-                for (int a = 0; a < NUM_A; ++a) tma_prefetch_l2(ma, kx, a_row + a * p.a_step);
-                if (++pf_kb == num_kb) {
-                    pf_kb = 0;
-                    pf_u += gridDim.x;
-                    if (pf_u < U) pf_t = decode_unit<BN, C::FEAT>(pf_u, mpre, offs, E, n_tiles, U, U2, p.rows2);
-                }
-            };
-            for (int i = 0; i < C::PF; ++i) prefetch_next();
             for (int u = blockIdx.x; u < U && !*abort_flag; u += gridDim.x) {
                 const Unit t = decode_unit<BN, C::FEAT>(u, mpre, offs, E, n_tiles, U, U2, p.rows2);
                 const CUtensorMap* ma = t.second ? &tm_a2 : &tm_a;
@@ -477,7 +442,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             row += h;
                         }
                     }
-                    prefetch_next();
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
