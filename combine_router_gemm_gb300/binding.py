@@ -338,10 +338,71 @@ class MoELayer:
         return layer_args(x, w["w_router"], w["bias"], w["w13"], w["w2"], w["w13_sh"],
                           w["w2_sh"], self.cfg, **outs)
 
-    def forward(self, x, out=None, **outs):
+    def forward(self, x, out=None, stream=None, **outs):
+        """out [T,d] fp32 for x [T,d] (device tensors), enqueued on `stream`
+        (default: the current stream)."""
         if x.shape[0] != self.T:
             raise ValueError(f"layer built for T={self.T}, got {x.shape[0]}")
         if out is None:
             out = torch.empty((x.shape[0], x.shape[1]), dtype=torch.float32, device=x.device)
-        moe_layer(self._args(x, **outs), out, self.ws, stream2=self.stream2)
+        moe_layer(self._args(x, **outs), out, self.ws, stream=stream, stream2=self.stream2)
         return out
+
+    def forward_host(self, host_inputs, host_outputs):
+        """Run the layer over a sequence of host batches, pipelined.
+
+        ``host_inputs[i]`` ([T,d], pinned host memory, the layer's dtype) is
+        copied in, the layer runs, and the result lands in ``host_outputs[i]``
+        ([T,d] fp32, pinned).  Copies in, compute and copies out run on three
+        streams with two device buffers each way, so that batch i+1's input
+        and batch i-1's output move while batch i computes.  Returns the
+        (first, last) CUDA events that bracket the whole sequence; the caller
+        synchronises.
+        """
+        n = len(host_inputs)
+        if n != len(host_outputs) or n == 0:
+            raise ValueError("need as many outputs as inputs (at least one)")
+        dev = self.ws.device
+        d = host_inputs[0].shape[1]
+        if not hasattr(self, "_pipe") or self._pipe["d"] != d:
+            self._pipe = dict(
+                d=d, x=[torch.empty((self.T, d), dtype=host_inputs[0].dtype, device=dev) for _ in range(2)],
+                out=[torch.empty((self.T, d), dtype=torch.float32, device=dev) for _ in range(2)],
+                s_in=torch.cuda.Stream(device=dev), s_comp=torch.cuda.Stream(device=dev),
+                s_out=torch.cuda.Stream(device=dev))
+        P = self._pipe
+        s_in, s_comp, s_out = P["s_in"], P["s_comp"], P["s_out"]
+        first = torch.cuda.Event(enable_timing=True)
+        last = torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream(dev)
+        for st in (s_in, s_comp, s_out):
+            st.wait_stream(cur)
+        first.record(s_in)
+        s_comp.wait_event(first)
+        s_out.wait_event(first)
+        done_comp = [None, None]  # compute of the batch that last used buffer b
+        done_out = [None, None]   # output copy of the batch that last used buffer b
+        for i in range(n):
+            b = i % 2
+            if done_comp[b] is not None:
+                s_in.wait_event(done_comp[b])  # x[b] is free once its compute ran
+            with torch.cuda.stream(s_in):
+                P["x"][b].copy_(host_inputs[i], non_blocking=True)
+            ev_in = torch.cuda.Event()
+            ev_in.record(s_in)
+            s_comp.wait_event(ev_in)
+            if done_out[b] is not None:
+                s_comp.wait_event(done_out[b])  # out[b] is free once it was copied out
+            self.forward(P["x"][b], out=P["out"][b], stream=s_comp)
+            ev_c = torch.cuda.Event()
+            ev_c.record(s_comp)
+            done_comp[b] = ev_c
+            s_out.wait_event(ev_c)
+            with torch.cuda.stream(s_out):
+                host_outputs[i].copy_(P["out"][b], non_blocking=True)
+            ev_o = torch.cuda.Event()
+            ev_o.record(s_out)
+            done_out[b] = ev_o
+        last.record(s_out)
+        cur.wait_stream(s_out)
+        return first, last

@@ -120,3 +120,25 @@ def test_layer_full_size_sampled(oracle, name):
     del inp, out
     gc.collect()
     torch.cuda.empty_cache()
+
+
+def test_layer_forward_host_pipelined_matches_forward():
+    """Host batches through the pipelined path give the same results as
+    device-side forward() calls, batch by batch."""
+    cfg = SMALL_BF16[0]
+    inp = inputs.make_inputs(cfg, seed=3, device="cuda")
+    layer = B.MoELayer(inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"],
+                       inp["w2_sh"], B.cfg_from(cfg), cfg.T)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    xs = [torch.randn((cfg.T, cfg.d), generator=g, device="cuda").to(torch.bfloat16)
+          for _ in range(5)]
+    ref = [layer.forward(x).clone() for x in xs]
+    hin = [x.cpu().pin_memory() for x in xs]
+    hout = [torch.empty((cfg.T, cfg.d), dtype=torch.float32).pin_memory() for _ in xs]
+    layer.forward_host(hin, hout)
+    torch.cuda.synchronize()
+    for r, h in zip(ref, hout):
+        assert torch.equal(r.cpu(), h)
+    rc, detail = B.moe_check_error(layer.ws)
+    assert rc == B.OK, detail
