@@ -41,7 +41,14 @@
 namespace {
 
 constexpr int BM = 128;         // features per tile (MMA M)
-constexpr int BK = 64;          // K per stage: one 128-byte swizzle atom row
+// K per stage: one swizzle-atom row of bf16 (64 elements = 128 B with the
+// 128-byte swizzle, 32 elements = 64 B with the 64-byte swizzle)
+#ifndef MOE_BK
+#define MOE_BK 64
+#endif
+constexpr int BK = MOE_BK;
+static_assert(BK == 64 || BK == 32, "K slab of 64 or 32 bf16");
+constexpr int SWZ_BYTES = BK * 2;  // swizzle span = row bytes
 constexpr int B_BOX = 32;       // token rows per TMA box
 constexpr int A_TILE_BYTES = BM * BK * 2;      // 16 KB
 constexpr int B_BOX_BYTES = B_BOX * BK * 2;    // 4 KB
@@ -187,15 +194,16 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row
-// core-matrix groups 1024 bytes apart (stride byte offset), version 1.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+// tcgen05 shared-memory matrix descriptor: K-major, swizzle span SWZ_BYTES
+// (128 or 64 B), 8-row core-matrix groups 8 * SWZ_BYTES apart (stride byte
+// offset), version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw(uint32_t addr) {
     uint64_t d = 0;
     d |= (uint64_t)((addr & 0x3FFFFu) >> 4);  // start address
-    d |= (uint64_t)1 << 16;                   // leading byte offset (unused for SW128 K-major)
-    d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset
+    d |= (uint64_t)1 << 16;                   // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)((8 * SWZ_BYTES) >> 4) << 32;  // stride byte offset
     d |= (uint64_t)1 << 46;                   // descriptor version
-    d |= (uint64_t)2 << 61;                   // swizzle: 128 B
+    d |= (uint64_t)(SWZ_BYTES == 128 ? 2 : 4) << 61;  // swizzle: 128 B or 64 B
     return d;
 }
 
@@ -543,13 +551,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t bsm = st + NUM_A * A_TILE_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t bdesc = smem_desc_sw128(bsm + kk * 32);
+                        const uint64_t bdesc = smem_desc_sw(bsm + kk * 32);
 #pragma unroll
                         for (int a = 0; a < NUM_A; ++a) {
                             const uint32_t dst = C::SPLIT_ACC ? d0 + (uint32_t)(a * BN) : d0;
                             // the first product into an accumulator overwrites it
                             const bool first = kb == 0 && kk == 0 && (C::SPLIT_ACC || a == 0);
-                            mma_bf16(dst, smem_desc_sw128(st + a * A_TILE_BYTES + kk * 32), bdesc,
+                            mma_bf16(dst, smem_desc_sw(st + a * A_TILE_BYTES + kk * 32), bdesc,
                                      idesc, first ? 0u : 1u);
                         }
                     }
@@ -718,7 +726,8 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
     cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     SWZ_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
