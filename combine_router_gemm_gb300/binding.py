@@ -328,8 +328,10 @@ class MoELayer:
         self.T = T
         dev = w13.device
         d = w13.shape[2]
-        probe = torch.empty((T, d), dtype=w13.dtype, device=dev)
-        self.ws_bytes = moe_layer_workspace_size(self._args(probe))
+        I_sh = w2_sh.shape[1] if w2_sh is not None else 0
+        sizes = LayerArgs(None, None, None, None, None, None, None, T, d, w2.shape[2], I_sh,
+                          _dtype_code(w13), cfg, None, None, None, None, None)
+        self.ws_bytes = moe_layer_workspace_size(sizes)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.stream2 = torch.cuda.Stream(device=dev) if overlap and w13_sh is not None else None
 

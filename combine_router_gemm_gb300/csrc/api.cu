@@ -137,7 +137,7 @@ LayerWs carve_layer(const moe_layer_args* a, void* base) {
     w.xp = take(S * d * es);
     w.yp = static_cast<float*>(take(S * d * 4));
     w.h = take(S * I * es);
-    const bool sh = a->w13_sh && a->w2_sh && a->I_sh > 0;
+    const bool sh = a->I_sh > 0;  // a shared expert is present iff I_sh > 0
     w.ysh = sh ? static_cast<float*>(take((size_t)T * d * 4)) : nullptr;
     w.hsh = sh ? take((size_t)T * a->I_sh * es) : nullptr;
     w.disp = take(moe_launch::dispatch_ws_bytes(T, k, E));
@@ -146,12 +146,20 @@ LayerWs carve_layer(const moe_layer_args* a, void* base) {
     return w;
 }
 
-int check_layer(const moe_layer_args* a) {
+// Sizes and configuration only (what the workspace size depends on).
+int check_layer_sizes(const moe_layer_args* a) {
     if (!a) return MOE_ERR_INVALID_ARG;
     int rc = check_cfg(&a->route);
     if (rc != MOE_OK) return rc;
     if ((rc = check_dims(a->T, a->d, a->route.top_k)) != MOE_OK) return rc;
     if (!dtype_ok(a->dtype) || a->I < 8 || a->I % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (a->I_sh < 0 || (a->I_sh > 0 && a->I_sh % 8 != 0)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+int check_layer(const moe_layer_args* a) {
+    int rc = check_layer_sizes(a);
+    if (rc != MOE_OK) return rc;
     if (!a->x || !a->w_router || !a->w13 || !a->w2) return MOE_ERR_INVALID_ARG;
     if (!moe_host::aligned16(a->x) || !moe_host::aligned16(a->w_router) ||
         !moe_host::aligned16(a->w13) || !moe_host::aligned16(a->w2))
@@ -293,7 +301,7 @@ int moe_combine(const float* y_perm, const int32_t* slot_to_row, const float* to
 }
 
 size_t moe_layer_workspace_size(const moe_layer_args* a) {
-    if (check_layer(a) != MOE_OK) return 0;
+    if (check_layer_sizes(a) != MOE_OK) return 0;
     return carve_layer(a, nullptr).total;
 }
 
@@ -328,8 +336,10 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     const bool overlap = sh && !merged && s1 && s1 != s0;
     if (overlap) {
         if (cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ev_shared, cudaEventDisableTiming) != cudaSuccess)
+            cudaEventCreateWithFlags(&ev_shared, cudaEventDisableTiming) != cudaSuccess) {
+            if (ev_start) cudaEventDestroy(ev_start);
             return MOE_ERR_CUDA;
+        }
         if (cudaEventRecord(ev_start, s0) != cudaSuccess ||
             cudaStreamWaitEvent(s1, ev_start, 0) != cudaSuccess)
             rc = MOE_ERR_CUDA;

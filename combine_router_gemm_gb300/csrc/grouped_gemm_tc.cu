@@ -741,14 +741,18 @@ bool make_bmaps(BMaps* m, const void* base, uint64_t rows, uint64_t cols) {
 template <int MODE, int BN>
 int launch(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, const BMaps& b2,
            const Params& p, cudaStream_t s) {
-    static bool attr_done = false;
+    // the shared-memory limit is a per-device attribute of the kernel: set it
+    // once per device (setting it twice is harmless, so no lock is needed)
+    static bool attr_done[64] = {};
     const size_t smem = Cfg<MODE, BN>::SMEM;
-    if (!attr_done) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
         if (cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, BN>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
             return MOE_ERR_CUDA;
-        attr_done = true;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
     grouped_gemm_tc_kernel<MODE, BN><<<moe_host::num_sms(), NUM_THREADS, smem, s>>>(a, b, a2, b2, p);
     return moe_host::launch_status();

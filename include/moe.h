@@ -190,7 +190,10 @@ typedef struct {
     void* const* stage_events; /* MOE_LAYER_EVENTS cudaEvent_t, or NULL */
 } moe_layer_args;
 
-/* Workspace bytes moe_layer needs. */
+/* Workspace bytes moe_layer needs (0 for invalid sizes or configuration).
+ * Only the sizes, dtype, routing configuration, I_sh (> 0: shared expert
+ * present) and which optional outputs are non-NULL matter here; the input
+ * pointers may still be NULL. */
 size_t moe_layer_workspace_size(const moe_layer_args* a);
 
 /* out [T,d] fp32 = the layer: route, dispatch, grouped FFN, shared expert,

@@ -138,3 +138,8 @@ def test_layer_rejects(lib):
     assert lib.moe_layer(ctypes.byref(args(I=100)), P, P, need, None, None) == B.ERR_INVALID_ARG
     assert lib.moe_layer(ctypes.byref(args()), None, P, need, None, None) == B.ERR_INVALID_ARG
     assert lib.moe_layer_workspace_size(ctypes.byref(args(dtype=3))) == 0
+    # the size query needs sizes only
+    assert lib.moe_layer_workspace_size(ctypes.byref(args(x=None, w13=None, w2=None,
+                                                          w_router=None))) == need
+    # the optional outputs replace workspace regions
+    assert lib.moe_layer_workspace_size(ctypes.byref(args(scores_out=P))) < need

@@ -142,3 +142,44 @@ def test_layer_forward_host_pipelined_matches_forward():
         assert torch.equal(r.cpu(), h)
     rc, detail = B.moe_check_error(layer.ws)
     assert rc == B.OK, detail
+
+
+EDGE = [
+    # a single token
+    (inputs.MoEConfig("edge_one_token", T=1, d=256, E=32, k=4, I=128, dtype="bf16",
+                      score_fn="sigmoid", n_group=4, topk_group=2, routed_scale=2.5, shared_I=128,
+                      bias="normal", expert_std=0.06, router_std=0.06), None),
+    # one dense expert (E = k = 1): the layer is a single SwiGLU MLP
+    (inputs.MoEConfig("edge_dense", T=257, d=128, E=1, k=1, I=256, dtype="bf16",
+                      expert_std=0.06), None),
+    # every token forced onto the same four experts; the other 28 have NaN
+    # weights, which must never be read
+    (inputs.MoEConfig("edge_forced", T=600, d=256, E=32, k=4, I=128, dtype="bf16",
+                      score_fn="sigmoid", n_group=1, topk_group=1, routed_scale=1.0, shared_I=0,
+                      bias="normal", expert_std=0.06, router_std=0.06), [3, 9, 17, 30]),
+]
+
+
+@pytest.mark.parametrize("cfg,forced", EDGE, ids=lambda v: getattr(v, "name", "f"))
+def test_layer_edge_cases(oracle, cfg, forced):
+    inp = inputs.make_inputs(cfg, seed=5, device="cuda")
+    if forced is not None:
+        inp["bias"] = torch.full((cfg.E,), -5.0, device="cuda")
+        inp["bias"][forced] = 5.0
+        rest = [e for e in range(cfg.E) if e not in forced]
+        ref_w13, ref_w2 = inp["w13"].clone(), inp["w2"].clone()
+        inp["w13"][rest] = float("nan")
+        inp["w2"][rest] = float("nan")
+    out, idx, w, scores, offs = run_layer(cfg, inp)
+    assert torch.isfinite(out).all()
+    if forced is not None:
+        assert sorted(np.unique(np_(idx)).tolist()) == sorted(forced)
+        counts = np.diff(np_(offs))
+        assert (counts[forced] == cfg.T).all() and counts.sum() == cfg.S
+        inp["w13"], inp["w2"] = ref_w13, ref_w2  # the oracle reads only selected experts anyway
+    sc, ridx, rw, rout = oracle_tokens(oracle, cfg, inp, torch.arange(cfg.T, device="cuda"))
+    same = (np_(idx) == ridx).all(1)
+    amb = near_tie_tokens(sc, np_(inp["bias"]), cfg.k, cfg.n_group, cfg.topk_group,
+                          abs_margin=tc_router_atol(cfg.d))
+    assert (same | amb).all()
+    assert_bf16_close(np_(out)[same], rout[same], cfg.name)
