@@ -50,9 +50,9 @@ def launches_per_step(cfg) -> int:
 # scaled x8 (experts and tokens) and the shared expert's weights are not
 # (profiles/grouped_gemm_tc_dsv3_prefill_e32.md).  Reported as null once the
 # kernel source no longer matches the captured one.
-TRAFFIC = {"source_sha256": "f4c1b69153bd0e59fdaf7228afb9afbb8e3ea6da16499ac86bacbde168c97369",
-           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 2.087113e9,
-                                            "dsv3_prefill": 8 * (2.087113e9 - 0.0587e9) + 0.0587e9}}
+TRAFFIC = {"source_sha256": "e0ce3365da40382c797e87f921e05ccd296241ae6453082986aae15c6c595162",
+           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 2.087016e9,
+                                            "dsv3_prefill": 8 * (2.087016e9 - 0.0587e9) + 0.0587e9}}
 
 
 def peaks():
