@@ -32,7 +32,12 @@ int num_sms() {
 
 namespace {
 
-constexpr size_t ERR_BYTES = 256;  // error word region at the start of a workspace
+// Workspace header: the error word, then zeroed counters of the grouped
+// GEMMs' dynamic unit schedule (one per launch that may be in flight).
+constexpr size_t ERR_BYTES = 256;
+constexpr int CTR_ROUTER = 1, CTR_FFN = 2 /* +1 */, CTR_SHARED = 4 /* +1 */;
+constexpr size_t HDR_CLEAR = 64;  // bytes of the header cleared per call
+unsigned* ctr(void* ws, int i) { return static_cast<unsigned*>(ws) + i; }
 
 size_t al(size_t v) { return (v + 255) / 256 * 256; }
 
@@ -67,14 +72,14 @@ size_t ffn_ws(int rows, int d, int I, int dtype) {
 
 int run_ffn(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
             const void* w13, const void* w2, int dtype, float* y, void* h, uint32_t* err,
-            cudaStream_t s, cudaEvent_t between = nullptr) {
+            unsigned* work, cudaStream_t s, cudaEvent_t between = nullptr) {
     if (rows == 0) {
         if (between && cudaEventRecord(between, s) != cudaSuccess) return MOE_ERR_CUDA;
         return MOE_OK;
     }
     if (dtype == MOE_BF16)
-        return moe_tc::grouped_ffn_bf16(x_perm, offsets, E, rows, d, I, w13, w2, y, h, err, s,
-                                        between);
+        return moe_tc::grouped_ffn_bf16(x_perm, offsets, E, rows, d, I, w13, w2, y, h, err, work,
+                                        s, between);
     int rc = moe_f32::grouped_ffn_f32(static_cast<const float*>(x_perm), offsets, E, rows, d, I,
                                       static_cast<const float*>(w13), static_cast<const float*>(w2),
                                       y, static_cast<float*>(h), err, s);
@@ -89,10 +94,10 @@ size_t route_ws(int E, int d, int dtype) {
 // bf16 activations: tcgen05 GEMM against the fp32 router weight split into
 // three bf16 terms; fp32 activations: fp32 CUDA-core GEMM.
 int run_router(const void* x, int dtype, const float* w_router, int T, int d, int E, int score_fn,
-               float* scores, void* wsplit, uint32_t* err, cudaStream_t s) {
+               float* scores, void* wsplit, uint32_t* err, unsigned* work, cudaStream_t s) {
     if (dtype == MOE_BF16)
         return moe_tc::router_bf16(x, w_router, T, d, E, score_fn == MOE_SCORE_SIGMOID, scores,
-                                   wsplit, err, s);
+                                   wsplit, err, work, s);
     return moe_launch::router_gemm(x, dtype, w_router, T, d, E, score_fn, scores, s);
 }
 
@@ -226,10 +231,10 @@ int moe_route(const void* x, int dtype, const float* w_router, const float* bias
         return MOE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t* err = static_cast<uint32_t*>(ws);
-    if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(ws, 0, HDR_CLEAR, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (T == 0) return MOE_OK;
     rc = run_router(x, dtype, w_router, T, d, cfg->num_experts, cfg->score_fn, scores,
-                    static_cast<char*>(ws) + ERR_BYTES, err, s);
+                    static_cast<char*>(ws) + ERR_BYTES, err, ctr(ws, CTR_ROUTER), s);
     if (rc != MOE_OK) return rc;
     return moe_launch::topk(scores, bias, T, cfg, topk_idx, topk_w, s);
 }
@@ -282,9 +287,9 @@ int moe_grouped_ffn(const void* x_perm, const int32_t* offsets, int E, int rows,
     if (!ws || ws_bytes < ffn_ws(rows, d, I, dtype)) return MOE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t* err = static_cast<uint32_t*>(ws);
-    if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(ws, 0, HDR_CLEAR, s) != cudaSuccess) return MOE_ERR_CUDA;
     return run_ffn(x_perm, offsets, E, rows, d, I, w13, w2, dtype, y_perm,
-                   static_cast<char*>(ws) + ERR_BYTES, err, s);
+                   static_cast<char*>(ws) + ERR_BYTES, err, ctr(ws, CTR_FFN), s);
 }
 
 int moe_combine(const float* y_perm, const int32_t* slot_to_row, const float* topk_w,
@@ -316,7 +321,7 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     const int T = a->T, d = a->d, I = a->I, E = a->route.num_experts, k = a->route.top_k;
     cudaStream_t s0 = static_cast<cudaStream_t>(stream);
     cudaStream_t s1 = static_cast<cudaStream_t>(stream2);
-    if (cudaMemsetAsync(w.err, 0, sizeof(uint32_t), s0) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(w.err, 0, HDR_CLEAR, s0) != cudaSuccess) return MOE_ERR_CUDA;
     if (T == 0) return MOE_OK;
     const bool sh = w.ysh != nullptr;
     cudaEvent_t stage[MOE_LAYER_EVENTS] = {};
@@ -345,12 +350,12 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
             rc = MOE_ERR_CUDA;
         if (rc == MOE_OK)
             rc = run_ffn(a->x, nullptr, 1, T, d, a->I_sh, a->w13_sh, a->w2_sh, a->dtype, w.ysh, w.hsh,
-                         w.err, s1);
+                         w.err, ctr(w.err, CTR_SHARED), s1);
         if (rc == MOE_OK && cudaEventRecord(ev_shared, s1) != cudaSuccess) rc = MOE_ERR_CUDA;
     }
     if (rc == MOE_OK)
         rc = run_router(a->x, a->dtype, a->w_router, T, d, E, a->route.score_fn, w.scores, w.wsplit,
-                        w.err, s0);
+                        w.err, ctr(w.err, CTR_ROUTER), s0);
     mark(1);
     if (rc == MOE_OK) rc = moe_launch::topk(w.scores, a->bias, T, &a->route, w.idx, w.w, s0);
     mark(2);
@@ -361,15 +366,15 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     if (rc == MOE_OK) {
         if (merged)
             rc = moe_tc::grouped_ffn_bf16(w.xp, w.offsets, E, T * k, d, I, a->w13, a->w2, w.yp, w.h,
-                                          w.err, s0, stage[4], &shx);
+                                          w.err, ctr(w.err, CTR_FFN), s0, stage[4], &shx);
         else
             rc = run_ffn(w.xp, w.offsets, E, T * k, d, I, a->w13, a->w2, a->dtype, w.yp, w.h,
-                         w.err, s0, stage[4]);
+                         w.err, ctr(w.err, CTR_FFN), s0, stage[4]);
     }
     mark(5);
     if (rc == MOE_OK && sh && !merged && !overlap)
         rc = run_ffn(a->x, nullptr, 1, T, d, a->I_sh, a->w13_sh, a->w2_sh, a->dtype, w.ysh, w.hsh,
-                     w.err, s0);
+                     w.err, ctr(w.err, CTR_SHARED), s0);
     if (rc == MOE_OK && overlap && cudaStreamWaitEvent(s0, ev_shared, 0) != cudaSuccess)
         rc = MOE_ERR_CUDA;
     if (rc == MOE_OK)

@@ -69,14 +69,16 @@ struct SharedExpert {
     void* h;          // [T,I] bf16 scratch
     float* y;         // [T,d] fp32 out
 };
+// work: two zeroed counters (gate/up launch, down launch) for the dynamic
+// unit schedule
 int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
                      const void* w13, const void* w2, float* y, void* h, uint32_t* err,
-                     cudaStream_t s, cudaEvent_t between = nullptr,
+                     unsigned* work, cudaStream_t s, cudaEvent_t between = nullptr,
                      const SharedExpert* sh = nullptr);
 size_t router_ws_bytes(int E, int d);
 int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s);
 int router_bf16(const void* x, const float* w_router, int T, int d, int E, int sigmoid,
-                float* scores, void* ws, uint32_t* err, cudaStream_t s);
+                float* scores, void* ws, uint32_t* err, unsigned* work, cudaStream_t s);
 }  // namespace moe_tc
 
 // ---- internal launchers (one per kernel family), used by api.cu -----------

@@ -53,6 +53,7 @@ constexpr int B_BOX = 32;       // token rows per TMA box
 constexpr int A_TILE_BYTES = BM * BK * 2;      // 16 KB
 constexpr int B_BOX_BYTES = B_BOX * BK * 2;    // 4 KB
 constexpr int NUM_EPI_WARPS = 8;  // two per 32-lane quarter of tensor memory
+constexpr int RING = 4;           // unit indices in flight from producer to consumers
 constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS);
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 1024;
@@ -131,6 +132,8 @@ struct Params {
     // dense segment of `rows2` rows through tm_a2/tm_b2 into out2
     int rows2;
     void* out2;
+    // zero before the launch: units past the first gridDim.x are claimed from it
+    unsigned* work;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -367,9 +370,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t* tfull_bar = bars + 2 * STAGES;    // [ACC]
     uint64_t* tempty_bar = tfull_bar + ACC;     // [ACC]
     uint64_t* drain_bar = tempty_bar + ACC;     // [1]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+    uint64_t* ufull_bar = drain_bar + 1;        // [RING] unit index published
+    uint64_t* uempty_bar = ufull_bar + RING;    // [RING] unit index read by all consumers
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(uempty_bar + RING);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* total_units = reinterpret_cast<int*>(tmem_slot + 2);
+    volatile int* ring = reinterpret_cast<volatile int*>(tmem_slot + 5);  // [RING]
     int* mpre = reinterpret_cast<int*>(smem + (size_t)STAGES * C::STAGE_BYTES + 256);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -434,6 +440,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(smem_u32(&tempty_bar[a]), NUM_EPI_WARPS);
         }
         mbar_init(smem_u32(drain_bar), 1);
+        for (int r = 0; r < RING; ++r) {
+            mbar_init(smem_u32(&ufull_bar[r]), 1);
+            mbar_init(smem_u32(&uempty_bar[r]), 1 + NUM_EPI_WARPS);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tm_a);
         for (int i = 0; i < 4; ++i) tma_prefetch_desc(&tm_b.m[i]);
@@ -472,7 +482,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             long issued = 0;
-            for (int u = blockIdx.x; u < U && !*abort_flag; u += gridDim.x) {
+            int slot = 0;
+            uint32_t uphase = 0;
+            // first unit: blockIdx.x; later ones: claimed from the launch's
+            // counter, so CTAs that finish early take more of the work
+            for (int u = blockIdx.x;;) {
+                // publish u (or the end, -1) to the MMA and epilogue warps
+                if (!mbar_wait(smem_u32(&uempty_bar[slot]), uphase ^ 1, abort_flag, p.err,
+                               moe::WAIT_LIMIT_NS))
+                    break;
+                const bool last = u >= U || *abort_flag;
+                ring[slot] = last ? -1 : u;
+                mbar_arrive(smem_u32(&ufull_bar[slot]));
+                if (++slot == RING) { slot = 0; uphase ^= 1; }
+                if (last) break;
+                const int next = (int)gridDim.x + (int)atomicAdd(p.work, 1u);
                 const Unit t = decode_unit<BN, C::FEAT>(u, sched);
                 const CUtensorMap* ma = t.second ? &tm_a2 : &tm_a;
                 const CUtensorMap* mb = t.second ? tm_b2.m : tm_b.m;
@@ -509,6 +533,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
+                u = next;
             }
             if (*abort_flag) {
                 // let the copies this thread started land before the CTA exits
@@ -530,7 +555,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool issued_any = false;
-            for (int u = blockIdx.x; u < U && !*abort_flag; u += gridDim.x) {
+            int slot = 0;
+            uint32_t uphase = 0;
+            while (!*abort_flag) {
+                if (!mbar_wait(smem_u32(&ufull_bar[slot]), uphase, abort_flag, p.err,
+                               moe::WAIT_LIMIT_NS))
+                    break;
+                const int u = ring[slot];
+                mbar_arrive(smem_u32(&uempty_bar[slot]));
+                if (++slot == RING) { slot = 0; uphase ^= 1; }
+                if (u < 0) break;
                 const Unit t = decode_unit<BN, C::FEAT>(u, sched);
                 const int bn = (t.n_tok + 15) & ~15;
                 const uint32_t idesc = idesc_bf16(bn);
@@ -586,7 +620,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int sub = (warp - 2) >> 2;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int u = blockIdx.x; u < U; u += gridDim.x) {
+        int slot = 0;
+        uint32_t uphase = 0;
+        while (true) {
+            int u = -1;
+            if (lane == 0 && mbar_wait(smem_u32(&ufull_bar[slot]), uphase, abort_flag, p.err,
+                                       moe::WAIT_LIMIT_NS)) {
+                u = ring[slot];
+                mbar_arrive(smem_u32(&uempty_bar[slot]));
+            }
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (++slot == RING) { slot = 0; uphase ^= 1; }
+            if (u < 0) break;
             const Unit t = decode_unit<BN, C::FEAT>(u, sched);
             if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.err,
                            moe::WAIT_LIMIT_NS))
@@ -767,7 +812,8 @@ namespace moe_tc {
 // expert (dense over sh->x, I_sh == I) runs inside the same two launches.
 int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
                      const void* w13, const void* w2, float* y, void* h, uint32_t* err,
-                     cudaStream_t s, cudaEvent_t between, const SharedExpert* sh) {
+                     unsigned* work, cudaStream_t s, cudaEvent_t between,
+                     const SharedExpert* sh) {
     if (E > MAX_E) return MOE_ERR_UNSUPPORTED;
     CUtensorMap a1, a2, a1s, a2s;
     BMaps b1, b2, b1s, b2s;
@@ -782,8 +828,10 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     } else {
         a1s = a1; b1s = b1; a2s = a2; b2s = b2;
     }
-    Params p1{offsets, E, rows, d, I, 2 * I, I, h, err, 0, two ? sh->T : 0, two ? sh->h : nullptr};
-    Params p2{offsets, E, rows, I, d, d, BM, y, err, 0, two ? sh->T : 0, two ? sh->y : nullptr};
+    Params p1{offsets, E, rows, d, I, 2 * I, I, h, err, 0, two ? sh->T : 0, two ? sh->h : nullptr,
+              work};
+    Params p2{offsets, E, rows, I, d, d, BM, y, err, 0, two ? sh->T : 0, two ? sh->y : nullptr,
+              work + 1};
     // Token tile per launch, from the average rows per expert (the host does
     // not see the device-side offsets).  A 128-row tile leaves room for one
     // more shared-memory stage, so more weight bytes in flight (and, for
@@ -812,7 +860,7 @@ size_t router_ws_bytes(int E, int d) { return (size_t)3 * E * d * 2; }
 // scores[T,E] = x W^T (fp32 accumulate) with W split into three bf16 terms;
 // sigmoid applied in the epilogue when asked.  ws: router_ws_bytes(E, d).
 int router_bf16(const void* x, const float* w_router, int T, int d, int E, int sigmoid,
-                float* scores, void* ws, uint32_t* err, cudaStream_t s) {
+                float* scores, void* ws, uint32_t* err, unsigned* work, cudaStream_t s) {
     __nv_bfloat16* wsplit = static_cast<__nv_bfloat16*>(ws);
     const long n = (long)E * d;
     const int blocks = (int)std::min<long>((n + 255) / 256, 4L * moe_host::num_sms());
@@ -822,7 +870,7 @@ int router_bf16(const void* x, const float* w_router, int T, int d, int E, int s
     CUtensorMap a;
     BMaps b;
     if (!make_map(&a, wsplit, 3ull * E, d, BM) || !make_bmaps(&b, x, T, d)) return MOE_ERR_CUDA;
-    Params p{nullptr, 1, T, d, E, 0, E, scores, err, sigmoid ? 1 : 0, 0, nullptr};
+    Params p{nullptr, 1, T, d, E, 0, E, scores, err, sigmoid ? 1 : 0, 0, nullptr, work};
     return launch<2, 64>(a, b, a, b, p, s);
 }
 
