@@ -105,6 +105,8 @@ struct Cand {
     int e;  // -1: none
 };
 
+constexpr int FAST_GROUPS = 8;  // group counts up to this take the all-at-once path
+
 __device__ __forceinline__ Cand better(Cand a, Cand b) {
     if (b.e < 0) return a;
     if (a.e < 0) return b;
@@ -145,59 +147,91 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ sco
 
     if (n_group > 1) {
         const int gs = E / n_group;
-        float my_gscore = 0.f;
-        for (int g = 0; g < n_group; ++g) {
-            // two largest keys of group g (values only; their sum is symmetric)
-            float v1 = -FLT_MAX, v2 = -FLT_MAX;
-            bool h1 = false, h2 = false;
+        int gid[EPL];  // group of each held expert
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) gid[i] = (i * 32 + lane) / gs;
+        unsigned keep = 0;
+        if (n_group <= FAST_GROUPS) {
+            // All groups at once: each lane keeps the two largest of its own
+            // keys per group (-inf = none), then a butterfly merges the pairs
+            // across the warp.  Top-2 of a multiset by values only: the merge
+            // (max(a1,b1), max(min(a1,b1), max(a2,b2))) is exact, and every
+            // group has at least two members, so no -inf survives.
+            float g1[FAST_GROUPS], g2[FAST_GROUPS];
+#pragma unroll
+            for (int g = 0; g < FAST_GROUPS; ++g) g1[g] = g2[g] = -INFINITY;
 #pragma unroll
             for (int i = 0; i < EPL; ++i) {
-                const int e = i * 32 + lane;
-                if (!ok[i] || e / gs != g) continue;
-                const float v = key[i];
-                if (!h1 || v > v1) {
-                    v2 = v1; h2 = h1;
-                    v1 = v; h1 = true;
-                } else if (!h2 || v > v2) {
-                    v2 = v; h2 = true;
+#pragma unroll
+                for (int g = 0; g < FAST_GROUPS; ++g) {
+                    if (ok[i] && gid[i] == g) {
+                        const float v = key[i];
+                        g2[g] = fmaxf(g2[g], fminf(g1[g], v));
+                        g1[g] = fmaxf(g1[g], v);
+                    }
                 }
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
-                const float o1 = __shfl_xor_sync(0xffffffffu, v1, off);
-                const float o2 = __shfl_xor_sync(0xffffffffu, v2, off);
-                const bool p1 = __shfl_xor_sync(0xffffffffu, h1, off);
-                const bool p2 = __shfl_xor_sync(0xffffffffu, h2, off);
-                // merge two sorted pairs (v1 >= v2), (o1 >= o2), absent entries last
-                float n1, n2;
-                bool q1, q2;
-                if (!p1 || (h1 && v1 >= o1)) {
-                    n1 = v1; q1 = h1;
-                    // second: best of v2 and o1
-                    if (!p1 || (h2 && v2 >= o1)) { n2 = v2; q2 = h2; } else { n2 = o1; q2 = p1; }
-                } else {
-                    n1 = o1; q1 = p1;
-                    if (!p2 || (h1 && v1 >= o2)) { n2 = v1; q2 = h1; } else { n2 = o2; q2 = p2; }
+#pragma unroll
+                for (int g = 0; g < FAST_GROUPS; ++g) {
+                    const float o1 = __shfl_xor_sync(0xffffffffu, g1[g], off);
+                    const float o2 = __shfl_xor_sync(0xffffffffu, g2[g], off);
+                    g2[g] = fmaxf(fminf(g1[g], o1), fmaxf(g2[g], o2));
+                    g1[g] = fmaxf(g1[g], o1);
                 }
-                v1 = n1; v2 = n2; h1 = q1; h2 = q2;
             }
-            if (lane == g) my_gscore = v1 + v2;
-        }
-        unsigned keep = 0;
-        bool gtaken = false;
-        for (int r = 0; r < topk_group; ++r) {
-            Cand c;
-            c.v = my_gscore;
-            c.e = (lane < n_group && !gtaken) ? lane : -1;
-            c = warp_best(c);
-            if (lane == c.e) gtaken = true;
-            keep |= 1u << c.e;
+            // every lane now holds every group score: pick the best groups,
+            // ties to the lower group, without further communication
+            float gsc[FAST_GROUPS];
+#pragma unroll
+            for (int g = 0; g < FAST_GROUPS; ++g) gsc[g] = g1[g] + g2[g];
+            for (int r = 0; r < topk_group; ++r) {
+                int best = -1;
+                float bv = 0.f;
+#pragma unroll
+                for (int g = 0; g < FAST_GROUPS; ++g) {
+                    if (g < n_group && !((keep >> g) & 1u) && (best < 0 || gsc[g] > bv)) {
+                        best = g;
+                        bv = gsc[g];
+                    }
+                }
+                keep |= 1u << best;
+            }
+        } else {
+            float my_gscore = 0.f;
+            for (int g = 0; g < n_group; ++g) {
+                // two largest keys of group g (values only; their sum is symmetric)
+                float v1 = -INFINITY, v2 = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) {
+                    if (ok[i] && gid[i] == g) {
+                        v2 = fmaxf(v2, fminf(v1, key[i]));
+                        v1 = fmaxf(v1, key[i]);
+                    }
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float o1 = __shfl_xor_sync(0xffffffffu, v1, off);
+                    const float o2 = __shfl_xor_sync(0xffffffffu, v2, off);
+                    v2 = fmaxf(fminf(v1, o1), fmaxf(v2, o2));
+                    v1 = fmaxf(v1, o1);
+                }
+                if (lane == g) my_gscore = v1 + v2;
+            }
+            bool gtaken = false;
+            for (int r = 0; r < topk_group; ++r) {
+                Cand c;
+                c.v = my_gscore;
+                c.e = (lane < n_group && !gtaken) ? lane : -1;
+                c = warp_best(c);
+                if (lane == c.e) gtaken = true;
+                keep |= 1u << c.e;
+            }
         }
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            const int e = i * 32 + lane;
-            if (ok[i] && !((keep >> (e / gs)) & 1u)) ok[i] = false;
-        }
+        for (int i = 0; i < EPL; ++i)
+            if (ok[i] && !((keep >> gid[i]) & 1u)) ok[i] = false;
     }
 
     // softmax normaliser over all E logits
