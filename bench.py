@@ -319,8 +319,10 @@ def run_ours(args, cfg):
         dn_bytes += d * Is * es + T * Is * es + T * d * 4
         dn_flops += 2.0 * T * Is * d
     perm_bytes = T * d * es + S * d * es + S * 4 * 3 + S * 4
-    names = ["router", "topk", "dispatch", "gate_up_gemm", "down_gemm", "combine"]
-    stages = {n: {"ms": round(m, 4)} for n, m in zip(names, stage_ms)}
+    # stage 1 covers the router GEMM and top-k (top-k sums the router's
+    # partial logits), stage 2 is empty
+    names = ["route", "route_", "dispatch", "gate_up_gemm", "down_gemm", "combine"]
+    stages = {n: {"ms": round(m, 4)} for n, m in zip(names, stage_ms) if n != "route_"}
 
     def bw(b, ms):
         return b / (ms * 1e-3) / 1e9

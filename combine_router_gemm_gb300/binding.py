@@ -72,7 +72,7 @@ def load() -> ctypes.CDLL:
     lib.moe_version.restype = i32
     lib.moe_route_from_scores.argtypes = [P, P, i32, ctypes.POINTER(RouteCfg), P, P, P]
     lib.moe_route_from_scores.restype = i32
-    lib.moe_route_workspace_size.argtypes = [i32, i32, i32]
+    lib.moe_route_workspace_size.argtypes = [i32, i32, i32, i32]
     lib.moe_route_workspace_size.restype = sz
     lib.moe_route.argtypes = [P, i32, P, P, i32, i32, ctypes.POINTER(RouteCfg), P, P, P, P, sz, P]
     lib.moe_route.restype = i32
@@ -156,14 +156,14 @@ def moe_route_from_scores(scores, bias, cfg: RouteCfg, topk_idx, topk_w, stream=
     _check(rc, "moe_route_from_scores")
 
 
-def moe_route_workspace_size(E: int, d: int, dtype: int) -> int:
-    return load().moe_route_workspace_size(E, d, dtype)
+def moe_route_workspace_size(T: int, E: int, d: int, dtype: int) -> int:
+    return load().moe_route_workspace_size(T, E, d, dtype)
 
 
 def moe_route(x, w_router, bias, cfg: RouteCfg, scores, topk_idx, topk_w, ws=None, stream=None):
     T, d = x.shape
     if ws is None:
-        ws = torch.empty(moe_route_workspace_size(cfg.num_experts, d, _dtype_code(x)),
+        ws = torch.empty(moe_route_workspace_size(T, cfg.num_experts, d, _dtype_code(x)),
                          dtype=torch.uint8, device=x.device)
     rc = load().moe_route(_ptr(x, None, "x"), _dtype_code(x), _ptr(w_router, torch.float32, "w_router"),
                           _ptr(bias, torch.float32, "bias"), T, d, ctypes.byref(cfg),

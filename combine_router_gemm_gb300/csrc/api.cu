@@ -87,18 +87,28 @@ int run_ffn(const void* x_perm, const int32_t* offsets, int E, int rows, int d, 
     return rc;
 }
 
-size_t route_ws(int E, int d, int dtype) {
-    return ERR_BYTES + (dtype == MOE_BF16 ? al(moe_tc::router_ws_bytes(E, d)) : 0);
+size_t route_ws(int T, int E, int d, int dtype) {
+    return ERR_BYTES + (dtype == MOE_BF16 ? al(moe_tc::router_ws_bytes(T, E, d)) : 0);
 }
 
-// bf16 activations: tcgen05 GEMM against the fp32 router weight split into
-// three bf16 terms; fp32 activations: fp32 CUDA-core GEMM.
-int run_router(const void* x, int dtype, const float* w_router, int T, int d, int E, int score_fn,
-               float* scores, void* wsplit, uint32_t* err, unsigned* work, cudaStream_t s) {
-    if (dtype == MOE_BF16)
-        return moe_tc::router_bf16(x, w_router, T, d, E, score_fn == MOE_SCORE_SIGMOID, scores,
-                                   wsplit, err, work, s);
-    return moe_launch::router_gemm(x, dtype, w_router, T, d, E, score_fn, scores, s);
+// Scores, top-k and gates.  bf16 activations: tcgen05 GEMM against the fp32
+// router weight split into three bf16 terms, writing partial logits of K
+// parts that the top-k kernel sums (and passes through the sigmoid) into
+// `scores`; fp32 activations: fp32 CUDA-core GEMM writing `scores`.
+int run_route(const void* x, int dtype, const float* w_router, const float* bias, int T, int d,
+              const moe_route_cfg* cfg, float* scores, int32_t* idx, float* w, void* rws,
+              uint32_t* err, unsigned* work, cudaStream_t s) {
+    const int E = cfg->num_experts;
+    if (dtype == MOE_BF16) {
+        float* partial = nullptr;
+        int ks = 0;
+        int rc = moe_tc::router_bf16(x, w_router, T, d, E, rws, err, work, &partial, &ks, s);
+        if (rc != MOE_OK) return rc;
+        return moe_launch::topk(nullptr, bias, T, cfg, idx, w, s, partial, ks, scores);
+    }
+    int rc = moe_launch::router_gemm(x, dtype, w_router, T, d, E, cfg->score_fn, scores, s);
+    if (rc != MOE_OK) return rc;
+    return moe_launch::topk(scores, bias, T, cfg, idx, w, s);
 }
 
 struct LayerWs {
@@ -146,7 +156,7 @@ LayerWs carve_layer(const moe_layer_args* a, void* base) {
     w.ysh = sh ? static_cast<float*>(take((size_t)T * d * 4)) : nullptr;
     w.hsh = sh ? take((size_t)T * a->I_sh * es) : nullptr;
     w.disp = take(moe_launch::dispatch_ws_bytes(T, k, E));
-    w.wsplit = a->dtype == MOE_BF16 ? take(moe_tc::router_ws_bytes(E, d)) : nullptr;
+    w.wsplit = a->dtype == MOE_BF16 ? take(moe_tc::router_ws_bytes(T, E, d)) : nullptr;
     w.total = off;
     return w;
 }
@@ -212,9 +222,9 @@ int moe_route_from_scores(const float* scores, const float* bias, int T, const m
                             static_cast<cudaStream_t>(stream));
 }
 
-size_t moe_route_workspace_size(int E, int d, int dtype) {
-    if (E < 1 || d < 1 || !dtype_ok(dtype)) return 0;
-    return route_ws(E, d, dtype);
+size_t moe_route_workspace_size(int T, int E, int d, int dtype) {
+    if (T < 0 || E < 1 || d < 1 || !dtype_ok(dtype)) return 0;
+    return route_ws(T, E, d, dtype);
 }
 
 int moe_route(const void* x, int dtype, const float* w_router, const float* bias, int T, int d,
@@ -227,16 +237,14 @@ int moe_route(const void* x, int dtype, const float* w_router, const float* bias
         return MOE_ERR_INVALID_ARG;
     if (!moe_host::aligned16(x) || !moe_host::aligned16(w_router)) return MOE_ERR_INVALID_ARG;
     if (bias && cfg->score_fn == MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
-    if (!ws || !moe_host::aligned16(ws) || ws_bytes < route_ws(cfg->num_experts, d, dtype))
+    if (!ws || !moe_host::aligned16(ws) || ws_bytes < route_ws(T, cfg->num_experts, d, dtype))
         return MOE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    uint32_t* err = static_cast<uint32_t*>(ws);
     if (cudaMemsetAsync(ws, 0, HDR_CLEAR, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (T == 0) return MOE_OK;
-    rc = run_router(x, dtype, w_router, T, d, cfg->num_experts, cfg->score_fn, scores,
-                    static_cast<char*>(ws) + ERR_BYTES, err, ctr(ws, CTR_ROUTER), s);
-    if (rc != MOE_OK) return rc;
-    return moe_launch::topk(scores, bias, T, cfg, topk_idx, topk_w, s);
+    return run_route(x, dtype, w_router, bias, T, d, cfg, scores, topk_idx, topk_w,
+                     static_cast<char*>(ws) + ERR_BYTES, static_cast<uint32_t*>(ws),
+                     ctr(ws, CTR_ROUTER), s);
 }
 
 size_t moe_dispatch_workspace_size(int T, int k, int E) {
@@ -354,10 +362,9 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
         if (rc == MOE_OK && cudaEventRecord(ev_shared, s1) != cudaSuccess) rc = MOE_ERR_CUDA;
     }
     if (rc == MOE_OK)
-        rc = run_router(a->x, a->dtype, a->w_router, T, d, E, a->route.score_fn, w.scores, w.wsplit,
-                        w.err, ctr(w.err, CTR_ROUTER), s0);
+        rc = run_route(a->x, a->dtype, a->w_router, a->bias, T, d, &a->route, w.scores, w.idx, w.w,
+                       w.wsplit, w.err, ctr(w.err, CTR_ROUTER), s0);
     mark(1);
-    if (rc == MOE_OK) rc = moe_launch::topk(w.scores, a->bias, T, &a->route, w.idx, w.w, s0);
     mark(2);
     if (rc == MOE_OK)
         rc = moe_launch::dispatch(w.idx, a->x, a->dtype, T, d, k, E, w.counts, w.offsets, w.s2r,

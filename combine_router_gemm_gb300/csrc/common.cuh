@@ -75,18 +75,22 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
                      const void* w13, const void* w2, float* y, void* h, uint32_t* err,
                      unsigned* work, cudaStream_t s, cudaEvent_t between = nullptr,
                      const SharedExpert* sh = nullptr);
-size_t router_ws_bytes(int E, int d);
+size_t router_ws_bytes(int T, int E, int d);
 int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s);
-int router_bf16(const void* x, const float* w_router, int T, int d, int E, int sigmoid,
-                float* scores, void* ws, uint32_t* err, unsigned* work, cudaStream_t s);
+int router_bf16(const void* x, const float* w_router, int T, int d, int E, void* ws,
+                uint32_t* err, unsigned* work, float** partial, int* ksplit, cudaStream_t s);
 }  // namespace moe_tc
 
 // ---- internal launchers (one per kernel family), used by api.cu -----------
 namespace moe_launch {
 int router_gemm(const void* x, int dtype, const float* w_router, int T, int d, int E, int score_fn,
                 float* scores, cudaStream_t s);
+// Top-k and gates.  With partial != NULL the scores are first finalised:
+// logits = sum of the ksplit partial tensors (in order), scores = logits or
+// sigmoid(logits), written to scores (which is then an output).
 int topk(const float* scores, const float* bias, int T, const moe_route_cfg* cfg, int32_t* idx,
-         float* w, cudaStream_t s);
+         float* w, cudaStream_t s, const float* partial = nullptr, int ksplit = 0,
+         float* scores_out = nullptr);
 size_t dispatch_ws_bytes(int T, int k, int E);
 int lookback_probe(void* flags_zeroed, uint64_t limit_ns, uint32_t* err, cudaStream_t s);
 int dispatch(const int32_t* idx, const void* x, int dtype, int T, int d, int k, int E, int32_t* counts,

@@ -134,6 +134,9 @@ struct Params {
     void* out2;
     // zero before the launch: units past the first gridDim.x are claimed from it
     unsigned* work;
+    // router: the K range is split into ksplit parts, each a unit of its own;
+    // part ks writes its partial sums to out + ks * rows * N_out
+    int ksplit;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -463,7 +466,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int U = total_units[0];
+    // units handed out: work units x K parts (router only)
+    const int KS = MODE == 2 ? max(1, p.ksplit) : 1;
+    const int U = total_units[0] < 0 ? -1 : total_units[0] * KS;
 
     // offsets for decode: dense mode synthesises {0, rows}
     __shared__ int s_dense_offs[2];
@@ -474,7 +479,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     const int* offs = p.offsets ? p.offsets : s_dense_offs;
     const int num_kb = (p.K + BK - 1) / BK;
-    const Sched sched{pre_c, pre_s, offs, E, n_tiles, U, total_units[1], total_units[2], U2, p.rows2};
+    const int kb_per = (num_kb + KS - 1) / KS;  // k-blocks per K part
+    const Sched sched{pre_c, pre_s,         offs, E, n_tiles, total_units[0], total_units[1],
+                      total_units[2], U2,  p.rows2};
 
     if (U > 0 && warp == 0) {
         // ================= TMA producer (one thread) =================
@@ -497,14 +504,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (++slot == RING) { slot = 0; uphase ^= 1; }
                 if (last) break;
                 const int next = (int)gridDim.x + (int)atomicAdd(p.work, 1u);
-                const Unit t = decode_unit<BN, C::FEAT>(u, sched);
+                const Unit t = decode_unit<BN, C::FEAT>(u / KS, sched);
+                const int kb0 = (u % KS) * kb_per, kb1 = min(num_kb, kb0 + kb_per);
                 const CUtensorMap* ma = t.second ? &tm_a2 : &tm_a;
                 const CUtensorMap* mb = t.second ? tm_b2.m : tm_b.m;
                 const int nbox = (t.n_tok + B_BOX - 1) / B_BOX;
                 const uint32_t bytes = NUM_A * A_TILE_BYTES + nbox * B_BOX_BYTES;
                 const int a_row = (t.second ? 0 : t.e * p.a_rows) + t.n0;
                 bool ok = true;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, p.err,
                                    moe::WAIT_LIMIT_NS)) {
                         ok = false;
@@ -565,7 +573,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_arrive(smem_u32(&uempty_bar[slot]));
                 if (++slot == RING) { slot = 0; uphase ^= 1; }
                 if (u < 0) break;
-                const Unit t = decode_unit<BN, C::FEAT>(u, sched);
+                const Unit t = decode_unit<BN, C::FEAT>(u / KS, sched);
+                const int kb0 = (u % KS) * kb_per, kb1 = min(num_kb, kb0 + kb_per);
                 const int bn = (t.n_tok + 15) & ~15;
                 const uint32_t idesc = idesc_bf16(bn);
                 if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, abort_flag, p.err,
@@ -574,7 +583,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
                 const uint32_t d0 = tmem_base + (uint32_t)(acc * ACC_COLS);
                 bool ok = true;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&full_bar[stage]), phase, abort_flag, p.err,
                                    moe::WAIT_LIMIT_NS)) {
                         ok = false;
@@ -590,7 +599,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int a = 0; a < NUM_A; ++a) {
                             const uint32_t dst = C::SPLIT_ACC ? d0 + (uint32_t)(a * BN) : d0;
                             // the first product into an accumulator overwrites it
-                            const bool first = kb == 0 && kk == 0 && (C::SPLIT_ACC || a == 0);
+                            const bool first = kb == kb0 && kk == 0 && (C::SPLIT_ACC || a == 0);
                             mma_bf16(dst, smem_desc_sw(st + a * A_TILE_BYTES + kk * 32), bdesc,
                                      idesc, first ? 0u : 1u);
                         }
@@ -632,14 +641,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             u = __shfl_sync(0xffffffffu, u, 0);
             if (++slot == RING) { slot = 0; uphase ^= 1; }
             if (u < 0) break;
-            const Unit t = decode_unit<BN, C::FEAT>(u, sched);
+            const Unit t = decode_unit<BN, C::FEAT>(u / KS, sched);
             if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.err,
                            moe::WAIT_LIMIT_NS))
                 break;
             tc_fence_after();
             const int n = t.n0 + q * 32 + lane;
             const bool n_ok = n < p.N_out;
-            void* out = t.second ? p.out2 : p.out;
+            // router K parts write separate partial sums (KS is 1 elsewhere)
+            void* out = t.second ? p.out2
+                                 : static_cast<char*>(p.out) +
+                                       (size_t)(u % KS) * p.rows * p.N_out * sizeof(float);
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
             for (int c0 = 32 * sub; c0 < t.n_tok; c0 += 64) {
@@ -667,17 +679,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_ld32(tbase + BN + c0, mid);
                     tmem_ld32(tbase + 2 * BN + c0, lo);
                     tmem_wait_ld();
-                    float* Y = static_cast<float*>(out);
-                    const bool sig = p.flags & 1;
+                    float* Y = static_cast<float*>(out);  // this K part's partial logits
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int tok = c0 + j;
-                        if (n_ok && tok < t.n_tok) {
-                            float v = __uint_as_float(g[j]) +
-                                      (__uint_as_float(mid[j]) + __uint_as_float(lo[j]));
-                            if (sig) v = 1.0f / (1.0f + expf(-v));
-                            Y[(size_t)(t.m_start + tok) * p.N_out + n] = v;
-                        }
+                        if (n_ok && tok < t.n_tok)
+                            Y[(size_t)(t.m_start + tok) * p.N_out + n] =
+                                __uint_as_float(g[j]) +
+                                (__uint_as_float(mid[j]) + __uint_as_float(lo[j]));
                     }
                 } else {
                     uint32_t g2[32];
@@ -855,13 +864,22 @@ int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s) {
     return moe_host::launch_status();
 }
 
-size_t router_ws_bytes(int E, int d) { return (size_t)3 * E * d * 2; }
+// Router: weight split (3 bf16 terms) + partial logits of up to MAX_KSPLIT
+// K parts, each [T,E] fp32.
+constexpr int MAX_KSPLIT = 8;
+size_t router_ws_bytes(int T, int E, int d) {
+    const size_t split = ((size_t)3 * E * d * 2 + 255) / 256 * 256;
+    return split + (size_t)MAX_KSPLIT * T * E * 4;
+}
 
-// scores[T,E] = x W^T (fp32 accumulate) with W split into three bf16 terms;
-// sigmoid applied in the epilogue when asked.  ws: router_ws_bytes(E, d).
-int router_bf16(const void* x, const float* w_router, int T, int d, int E, int sigmoid,
-                float* scores, void* ws, uint32_t* err, unsigned* work, cudaStream_t s) {
+// Partial logits of x W^T (fp32 accumulate) with W split into three bf16
+// terms: K is cut into *ksplit parts (chosen so that the units fill the SMs),
+// part ks written to partial + ks * T * E.  ws: router_ws_bytes(T, E, d).
+int router_bf16(const void* x, const float* w_router, int T, int d, int E, void* ws,
+                uint32_t* err, unsigned* work, float** partial, int* ksplit, cudaStream_t s) {
     __nv_bfloat16* wsplit = static_cast<__nv_bfloat16*>(ws);
+    const size_t split = ((size_t)3 * E * d * 2 + 255) / 256 * 256;
+    float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + split);
     const long n = (long)E * d;
     const int blocks = (int)std::min<long>((n + 255) / 256, 4L * moe_host::num_sms());
     split_weight_kernel<<<blocks, 256, 0, s>>>(w_router, n, wsplit);
@@ -870,8 +888,15 @@ int router_bf16(const void* x, const float* w_router, int T, int d, int E, int s
     CUtensorMap a;
     BMaps b;
     if (!make_map(&a, wsplit, 3ull * E, d, BM) || !make_bmaps(&b, x, T, d)) return MOE_ERR_CUDA;
-    Params p{nullptr, 1, T, d, E, 0, E, scores, err, sigmoid ? 1 : 0, 0, nullptr, work};
-    return launch<2, 64>(a, b, a, b, p, s);
+    constexpr int RBN = 128;
+    const int units = ((T + RBN - 1) / RBN) * ((E + BM - 1) / BM);
+    const int num_kb = (d + BK - 1) / BK;
+    int ks = std::max(1, std::min(MAX_KSPLIT, moe_host::num_sms() / std::max(1, units)));
+    while (ks > 1 && num_kb / ks < 8) --ks;  // keep each part at least 8 k-blocks long
+    Params p{nullptr, 1, T, d, E, 0, E, part, err, 0, 0, nullptr, work, ks};
+    *partial = part;
+    *ksplit = ks;
+    return launch<2, RBN>(a, b, a, b, p, s);
 }
 
 }  // namespace moe_tc

@@ -130,18 +130,31 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ sco
                                                    const float* __restrict__ bias, int T, int E,
                                                    int k, int n_group, int topk_group, int sigmoid,
                                                    float scale, int32_t* __restrict__ idx_out,
-                                                   float* __restrict__ w_out) {
+                                                   float* __restrict__ w_out,
+                                                   const float* __restrict__ partial, int ksplit,
+                                                   float* __restrict__ scores_out) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
-    const float* s = scores + (size_t)t * E;
     float sc[EPL], key[EPL];
     bool ok[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
         const int e = i * 32 + lane;
         ok[i] = e < E;
-        sc[i] = ok[i] ? s[e] : 0.f;
+        if (partial) {
+            // scores from the router's K-part partial logits, summed in order
+            float v = 0.f;
+            if (ok[i]) {
+                v = partial[(size_t)t * E + e];
+                for (int ks = 1; ks < ksplit; ++ks) v += partial[((size_t)ks * T + t) * E + e];
+                if (sigmoid) v = 1.0f / (1.0f + expf(-v));
+                scores_out[(size_t)t * E + e] = v;
+            }
+            sc[i] = v;
+        } else {
+            sc[i] = ok[i] ? scores[(size_t)t * E + e] : 0.f;
+        }
         key[i] = ok[i] ? (bias ? sc[i] + bias[e] : sc[i]) : 0.f;
     }
 
@@ -301,13 +314,14 @@ int router_gemm(const void* x, int dtype, const float* w_router, int T, int d, i
 }
 
 int topk(const float* scores, const float* bias, int T, const moe_route_cfg* c, int32_t* idx,
-         float* w, cudaStream_t s) {
+         float* w, cudaStream_t s, const float* partial, int ksplit, float* scores_out) {
     const int E = c->num_experts;
     const int blocks = moe::ceil_div(T, 8);
     const int sig = c->score_fn == MOE_SCORE_SIGMOID;
 #define MOE_TOPK(EPL)                                                                          \
     topk_kernel<EPL><<<blocks, 256, 0, s>>>(scores, bias, T, E, c->top_k, c->n_group,          \
-                                            c->topk_group, sig, c->routed_scale, idx, w)
+                                            c->topk_group, sig, c->routed_scale, idx, w, partial, \
+                                            ksplit, scores_out)
     const int epl = moe::ceil_div(E, 32);
     if (epl <= 1) MOE_TOPK(1);
     else if (epl <= 2) MOE_TOPK(2);

@@ -94,8 +94,8 @@ int moe_route_from_scores(const float* scores, const float* bias, int T,
                           const moe_route_cfg* cfg, int32_t* topk_idx, float* topk_w,
                           void* stream);
 
-/* Workspace bytes moe_route needs (E experts, hidden size d). */
-size_t moe_route_workspace_size(int E, int d, int dtype);
+/* Workspace bytes moe_route needs (T tokens, E experts, hidden size d). */
+size_t moe_route_workspace_size(int T, int E, int d, int dtype);
 
 /* Router GEMM then moe_route_from_scores.
  *   x        [T,d] bf16 or fp32 (dtype)
@@ -104,8 +104,9 @@ size_t moe_route_workspace_size(int E, int d, int dtype);
  * bf16 x: tcgen05 tensor cores, with w_router split into three bf16 terms
  * (hi + mid + lo, each the bf16 rounding of what the previous leave) so that
  * every product is exact and sums are fp32 -- the result matches an fp32
- * GEMM to fp32 rounding.  fp32 x: CUDA cores in fp32.
- * ws: moe_route_workspace_size bytes (error word, split weight). */
+ * GEMM to fp32 rounding; the K range may be cut into parts whose partial sums
+ * are added (in order) before the sigmoid.  fp32 x: CUDA cores in fp32.
+ * ws: moe_route_workspace_size bytes (error word, split weight, partials). */
 int moe_route(const void* x, int dtype, const float* w_router, const float* bias, int T, int d,
               const moe_route_cfg* cfg, float* scores, int32_t* topk_idx, float* topk_w, void* ws,
               size_t ws_bytes, void* stream);
@@ -170,9 +171,10 @@ int moe_combine(const float* y_perm, const int32_t* slot_to_row, const float* to
  * when non-NULL, receive the intermediate routing results.
  * stage_events, when non-NULL, points to MOE_LAYER_EVENTS cudaEvent_t handles
  * (host array, caller-created) that moe_layer records on `stream` at: start,
- * after the router GEMM, after top-k, after dispatch, after the routed gate/up
- * GEMM, after the routed down GEMM, and at the end (after combine).  They
- * let a caller time each stage inside a run of the whole layer. */
+ * after routing (router GEMM, top-k and gates), once more at the same point
+ * (kept so that stage indices stay fixed), after dispatch, after the routed
+ * gate/up GEMM, after the routed down GEMM, and at the end (after combine).
+ * They let a caller time each stage inside a run of the whole layer. */
 typedef struct {
     const void* x;          /* [T,d]   */
     const float* w_router;  /* [E,d]   */

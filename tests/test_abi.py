@@ -80,8 +80,8 @@ def test_route_rejects_bad_pointers(lib):
     assert lib.moe_route_from_scores(None, None, 10, ctypes.byref(c), P, P, None) == B.ERR_INVALID_ARG
     # a bias with softmax routing has no meaning
     assert lib.moe_route_from_scores(P, P, 10, ctypes.byref(c), P, P, None) == B.ERR_INVALID_ARG
-    need = lib.moe_route_workspace_size(8, 64, B.BF16)
-    assert need >= 3 * 8 * 64 * 2
+    need = lib.moe_route_workspace_size(10, 8, 64, B.BF16)
+    assert need >= 3 * 8 * 64 * 2 + 10 * 8 * 4
     assert lib.moe_route(P + 4, B.BF16, P, None, 10, 64, ctypes.byref(c), P, P, P, P, need, None) == B.ERR_INVALID_ARG
     assert lib.moe_route(P, B.BF16, P, None, 10, 60, ctypes.byref(c), P, P, P, P, need, None) == B.ERR_INVALID_ARG
     assert lib.moe_route(P, 5, P, None, 10, 64, ctypes.byref(c), P, P, P, P, need, None) == B.ERR_INVALID_ARG
