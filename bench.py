@@ -266,7 +266,8 @@ def run_ours(args, cfg):
     pk = peaks()
     inp = inputs.make_inputs(cfg, seed=0, device="cuda")
     layer = B.MoELayer(inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"],
-                       inp["w2_sh"], B.cfg_from(cfg), cfg.T, overlap=not args.no_overlap)
+                       inp["w2_sh"], B.cfg_from(cfg), cfg.T, overlap=not args.no_overlap,
+                       fused_combine=args.fused_combine)
     x = inp["x"]
     out = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device="cuda")
     offs = torch.empty(cfg.E + 1, dtype=torch.int32, device="cuda")
@@ -409,6 +410,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-overlap", action="store_true", help="shared expert on the main stream")
+    ap.add_argument("--fused-combine", action="store_true",
+                    help="add the down projection's results straight into the output (atomics)")
     args = ap.parse_args()
     from combine_router_gemm_gb300 import inputs
     cfg = inputs.CONFIGS[args.config]

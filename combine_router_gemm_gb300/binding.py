@@ -48,7 +48,10 @@ class LayerArgs(ctypes.Structure):
                 ("I", ctypes.c_int32), ("I_sh", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("route", RouteCfg), ("scores_out", ctypes.c_void_p),
                 ("topk_idx_out", ctypes.c_void_p), ("topk_w_out", ctypes.c_void_p),
-                ("offsets_out", ctypes.c_void_p), ("stage_events", ctypes.c_void_p)]
+                ("offsets_out", ctypes.c_void_p), ("stage_events", ctypes.c_void_p),
+                ("flags", ctypes.c_int32)]
+
+LAYER_FUSED_COMBINE = 1
 
 LAYER_EVENTS = 7
 
@@ -245,7 +248,7 @@ def moe_combine(y_perm, slot_to_row, topk_w, shared, out, stream=None):
 
 def layer_args(x, w_router, bias, w13, w2, w13_sh, w2_sh, cfg: RouteCfg, scores_out=None,
                topk_idx_out=None, topk_w_out=None, offsets_out=None,
-               stage_events=None) -> LayerArgs:
+               stage_events=None, flags: int = 0) -> LayerArgs:
     """``stage_events``: None or a list of LAYER_EVENTS torch.cuda.Event (kept
     alive by the caller), recorded by the library at the stage boundaries."""
     T, d = x.shape
@@ -258,7 +261,7 @@ def layer_args(x, w_router, bias, w13, w2, w13_sh, w2_sh, cfg: RouteCfg, scores_
                      _ptr(scores_out, torch.float32, "scores_out"),
                      _ptr(topk_idx_out, torch.int32, "topk_idx_out"),
                      _ptr(topk_w_out, torch.float32, "topk_w_out"),
-                     _ptr(offsets_out, torch.int32, "offsets_out"), _events(stage_events))
+                     _ptr(offsets_out, torch.int32, "offsets_out"), _events(stage_events), flags)
 
 
 _event_arrays = {}
@@ -322,15 +325,16 @@ class MoELayer:
     """
 
     def __init__(self, w_router, bias, w13, w2, w13_sh, w2_sh, cfg: RouteCfg, T: int,
-                 overlap: bool = True):
+                 overlap: bool = True, fused_combine: bool = False):
         self.w = dict(w_router=w_router, bias=bias, w13=w13, w2=w2, w13_sh=w13_sh, w2_sh=w2_sh)
         self.cfg = cfg
         self.T = T
         dev = w13.device
         d = w13.shape[2]
         I_sh = w2_sh.shape[1] if w2_sh is not None else 0
+        self.flags = LAYER_FUSED_COMBINE if fused_combine else 0
         sizes = LayerArgs(None, None, None, None, None, None, None, T, d, w2.shape[2], I_sh,
-                          _dtype_code(w13), cfg, None, None, None, None, None)
+                          _dtype_code(w13), cfg, None, None, None, None, None, self.flags)
         self.ws_bytes = moe_layer_workspace_size(sizes)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.stream2 = torch.cuda.Stream(device=dev) if overlap and w13_sh is not None else None
@@ -338,7 +342,7 @@ class MoELayer:
     def _args(self, x, **outs):
         w = self.w
         return layer_args(x, w["w_router"], w["bias"], w["w13"], w["w2"], w["w13_sh"],
-                          w["w2_sh"], self.cfg, **outs)
+                          w["w2_sh"], self.cfg, flags=self.flags, **outs)
 
     def forward(self, x, out=None, stream=None, **outs):
         """out [T,d] fp32 for x [T,d] (device tensors), enqueued on `stream`

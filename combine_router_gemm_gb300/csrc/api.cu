@@ -127,6 +127,7 @@ struct LayerWs {
     void* hsh;
     void* disp;
     void* wsplit;
+    float* w_row;  // fused combine: gate weight of each permuted row
     size_t total;
 };
 
@@ -157,6 +158,7 @@ LayerWs carve_layer(const moe_layer_args* a, void* base) {
     w.hsh = sh ? take((size_t)T * a->I_sh * es) : nullptr;
     w.disp = take(moe_launch::dispatch_ws_bytes(T, k, E));
     w.wsplit = a->dtype == MOE_BF16 ? take(moe_tc::router_ws_bytes(T, E, d)) : nullptr;
+    w.w_row = (a->flags & MOE_LAYER_FUSED_COMBINE) ? static_cast<float*>(take(S * 4)) : nullptr;
     w.total = off;
     return w;
 }
@@ -189,6 +191,10 @@ int check_layer(const moe_layer_args* a) {
     const void* outs[] = {a->scores_out, a->topk_idx_out, a->topk_w_out, a->offsets_out};
     for (const void* o : outs)
         if (o && !moe_host::aligned16(o)) return MOE_ERR_INVALID_ARG;
+    if (a->flags & ~MOE_LAYER_FUSED_COMBINE) return MOE_ERR_INVALID_ARG;
+    if ((a->flags & MOE_LAYER_FUSED_COMBINE) &&
+        (a->dtype != MOE_BF16 || (a->I_sh > 0 && a->I_sh != a->I)))
+        return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 
@@ -366,14 +372,19 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
                        w.wsplit, w.err, ctr(w.err, CTR_ROUTER), s0);
     mark(1);
     mark(2);
+    const bool fused = a->flags & MOE_LAYER_FUSED_COMBINE;
     if (rc == MOE_OK)
         rc = moe_launch::dispatch(w.idx, a->x, a->dtype, T, d, k, E, w.counts, w.offsets, w.s2r,
-                                  w.r2t, w.xp, w.disp, w.err, s0);
+                                  w.r2t, w.xp, w.disp, w.err, s0, fused ? w.w : nullptr, w.w_row);
     mark(3);
+    if (rc == MOE_OK && fused && cudaMemsetAsync(out, 0, sizeof(float) * (size_t)T * d, s0) != cudaSuccess)
+        rc = MOE_ERR_CUDA;
+    const moe_tc::FusedCombine fc{out, w.r2t, w.w_row};
     if (rc == MOE_OK) {
-        if (merged)
+        if (merged || fused)
             rc = moe_tc::grouped_ffn_bf16(w.xp, w.offsets, E, T * k, d, I, a->w13, a->w2, w.yp, w.h,
-                                          w.err, ctr(w.err, CTR_FFN), s0, stage[4], &shx);
+                                          w.err, ctr(w.err, CTR_FFN), s0, stage[4],
+                                          merged ? &shx : nullptr, fused ? &fc : nullptr);
         else
             rc = run_ffn(w.xp, w.offsets, E, T * k, d, I, a->w13, a->w2, a->dtype, w.yp, w.h,
                          w.err, ctr(w.err, CTR_FFN), s0, stage[4]);
@@ -384,7 +395,7 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
                      w.err, ctr(w.err, CTR_SHARED), s0);
     if (rc == MOE_OK && overlap && cudaStreamWaitEvent(s0, ev_shared, 0) != cudaSuccess)
         rc = MOE_ERR_CUDA;
-    if (rc == MOE_OK)
+    if (rc == MOE_OK && !fused)
         rc = moe_launch::combine(w.yp, w.s2r, w.w, w.ysh, T, k, d, out, w.err, s0);
     mark(6);
     if (ev_start) cudaEventDestroy(ev_start);

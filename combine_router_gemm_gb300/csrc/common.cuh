@@ -71,10 +71,17 @@ struct SharedExpert {
 };
 // work: two zeroed counters (gate/up launch, down launch) for the dynamic
 // unit schedule
+// The down projection's results added straight into the layer output:
+// out[row_token[r]] += w_row[r] * y[r] (shared expert rows: weight 1).
+struct FusedCombine {
+    float* out;                // [T,d] fp32, zeroed before the launch
+    const int32_t* row_token;  // [rows]
+    const float* w_row;        // [rows]
+};
 int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
                      const void* w13, const void* w2, float* y, void* h, uint32_t* err,
                      unsigned* work, cudaStream_t s, cudaEvent_t between = nullptr,
-                     const SharedExpert* sh = nullptr);
+                     const SharedExpert* sh = nullptr, const FusedCombine* fc = nullptr);
 size_t router_ws_bytes(int T, int E, int d);
 int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s);
 int router_bf16(const void* x, const float* w_router, int T, int d, int E, void* ws,
@@ -93,9 +100,10 @@ int topk(const float* scores, const float* bias, int T, const moe_route_cfg* cfg
          float* scores_out = nullptr);
 size_t dispatch_ws_bytes(int T, int k, int E);
 int lookback_probe(void* flags_zeroed, uint64_t limit_ns, uint32_t* err, cudaStream_t s);
+// w_slot/w_row (both or neither): also write each permuted row's gate weight
 int dispatch(const int32_t* idx, const void* x, int dtype, int T, int d, int k, int E, int32_t* counts,
              int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_token, void* x_perm, void* ws,
-             uint32_t* err, cudaStream_t s);
+             uint32_t* err, cudaStream_t s, const float* w_slot = nullptr, float* w_row = nullptr);
 size_t ffn_ws_bytes(int rows, int I, int dtype);
 int grouped_ffn(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
                 const void* w13, const void* w2, int dtype, float* y, void* h_ws, uint32_t* err,

@@ -223,7 +223,8 @@ __global__ void __launch_bounds__(DISP_THREADS) dispatch_count_kernel(
 __global__ void __launch_bounds__(256) permute_kernel(
     const int32_t* __restrict__ idx, const int* __restrict__ pos, const int32_t* __restrict__ offsets,
     int S, int k, int E, const uint4* __restrict__ x, int row_vecs, int32_t* __restrict__ slot_to_row,
-    int32_t* __restrict__ row_to_token, uint4* __restrict__ x_perm, const uint32_t* err) {
+    int32_t* __restrict__ row_to_token, uint4* __restrict__ x_perm, const float* __restrict__ w_slot,
+    float* __restrict__ w_row, const uint32_t* err) {
     if (moe::read_error(err)) return;
     const int lane = threadIdx.x & 31;
     const int s = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(256) permute_kernel(
     if (lane == 0) {
         slot_to_row[s] = row;
         row_to_token[row] = t;
+        if (w_row) w_row[row] = w_slot[s];  // gate weight of the row (fused combine)
     }
     if (!x_perm) return;
     const uint4* src = x + (size_t)t * row_vecs;
@@ -264,7 +266,8 @@ size_t dispatch_ws_bytes(int T, int k, int E) { return ws_bytes(T * k, E); }
 
 int dispatch(const int32_t* idx, const void* x, int dtype, int T, int d, int k, int E,
              int32_t* counts, int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_token,
-             void* x_perm, void* ws, uint32_t* err, cudaStream_t s) {
+             void* x_perm, void* ws, uint32_t* err, cudaStream_t s, const float* w_slot,
+             float* w_row) {
     const int S = T * k;
     const int nb = moe::ceil_div(S, DISP_CH);
     DispatchWs st = carve(ws, S, E);
@@ -281,7 +284,7 @@ int dispatch(const int32_t* idx, const void* x, int dtype, int T, int d, int k, 
     const int row_vecs = (int)((size_t)d * esize / 16);
     permute_kernel<<<moe::ceil_div(S, 8), 256, 0, s>>>(
         idx, st.pos, offsets, S, k, E, static_cast<const uint4*>(x), row_vecs, slot_to_row,
-        row_to_token, static_cast<uint4*>(x_perm), err);
+        row_to_token, static_cast<uint4*>(x_perm), w_slot, w_row, err);
     return moe_host::launch_status();
 }
 

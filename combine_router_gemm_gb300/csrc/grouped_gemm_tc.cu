@@ -137,6 +137,12 @@ struct Params {
     // router: the K range is split into ksplit parts, each a unit of its own;
     // part ks writes its partial sums to out + ks * rows * N_out
     int ksplit;
+    // down projection with fused combine (comb_out != NULL): instead of
+    // writing y, add w_row[r] * y[r] into comb_out[row_token[r]] (routed
+    // rows) or y[r] into comb_out[r] (second problem)
+    float* comb_out;
+    const int32_t* row_token;
+    const float* w_row;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -692,16 +698,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     uint32_t g2[32];
                     tmem_ld32(tbase + BN + c0, g2);
                     tmem_wait_ld();
-                    float* Y = static_cast<float*>(out);
                     const int n2 = n + BM;  // the second feature tile
                     const bool n2_ok = n2 < p.N_out;
+                    if (p.comb_out) {
+                        // fused combine: weighted adds into the token's output row
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int tok = c0 + j;
-                        if (tok < t.n_tok) {
-                            float* row = Y + (size_t)(t.m_start + tok) * p.N_out;
-                            if (n_ok) row[n] = __uint_as_float(g[j]);
-                            if (n2_ok) row[n2] = __uint_as_float(g2[j]);
+                        for (int j = 0; j < 32; ++j) {
+                            const int tok = c0 + j;
+                            if (tok < t.n_tok) {
+                                const int r = t.m_start + tok;
+                                const int tk = t.second ? r : p.row_token[r];
+                                const float wgt = t.second ? 1.0f : p.w_row[r];
+                                float* row = p.comb_out + (size_t)tk * p.N_out;
+                                if (n_ok) atomicAdd(row + n, wgt * __uint_as_float(g[j]));
+                                if (n2_ok) atomicAdd(row + n2, wgt * __uint_as_float(g2[j]));
+                            }
+                        }
+                    } else {
+                        float* Y = static_cast<float*>(out);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int tok = c0 + j;
+                            if (tok < t.n_tok) {
+                                float* row = Y + (size_t)(t.m_start + tok) * p.N_out;
+                                if (n_ok) row[n] = __uint_as_float(g[j]);
+                                if (n2_ok) row[n2] = __uint_as_float(g2[j]);
+                            }
                         }
                     }
                 }
@@ -822,7 +844,7 @@ namespace moe_tc {
 int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
                      const void* w13, const void* w2, float* y, void* h, uint32_t* err,
                      unsigned* work, cudaStream_t s, cudaEvent_t between,
-                     const SharedExpert* sh) {
+                     const SharedExpert* sh, const FusedCombine* fc) {
     if (E > MAX_E) return MOE_ERR_UNSUPPORTED;
     CUtensorMap a1, a2, a1s, a2s;
     BMaps b1, b2, b1s, b2s;
@@ -840,7 +862,8 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     Params p1{offsets, E, rows, d, I, 2 * I, I, h, err, 0, two ? sh->T : 0, two ? sh->h : nullptr,
               work};
     Params p2{offsets, E, rows, I, d, d, BM, y, err, 0, two ? sh->T : 0, two ? sh->y : nullptr,
-              work + 1};
+              work + 1, 1, fc ? fc->out : nullptr, fc ? fc->row_token : nullptr,
+              fc ? fc->w_row : nullptr};
     // Token tile per launch, from the average rows per expert (the host does
     // not see the device-side offsets).  A 128-row tile leaves room for one
     // more shared-memory stage, so more weight bytes in flight (and, for

@@ -190,7 +190,15 @@ typedef struct {
     float* topk_w_out;      /* [T,k]  or NULL */
     int32_t* offsets_out;   /* [E+1]  or NULL */
     void* const* stage_events; /* MOE_LAYER_EVENTS cudaEvent_t, or NULL */
+    int32_t flags;          /* MOE_LAYER_* bits, 0 = defaults */
 } moe_layer_args;
+
+/* moe_layer_args.flags: add the down projection's results straight into `out`
+ * (fp32 atomic adds in the grouped GEMM's epilogue) instead of writing the
+ * permuted fp32 rows and combining them in a separate pass.  bf16 with the
+ * shared expert of the routed experts' size (or none) only.  The summation
+ * order then varies from run to run (results agree to fp32 rounding). */
+#define MOE_LAYER_FUSED_COMBINE 1
 
 /* Workspace bytes moe_layer needs (0 for invalid sizes or configuration).
  * Only the sizes, dtype, routing configuration, I_sh (> 0: shared expert

@@ -19,10 +19,11 @@ from helpers import (F32_REL_FRO, assert_bf16_close, cuda_f32, cuda_i32, near_ti
 pytestmark = pytest.mark.gpu
 
 
-def run_layer(cfg, inp, overlap=True):
+def run_layer(cfg, inp, overlap=True, fused_combine=False):
     T = cfg.T
     layer = B.MoELayer(inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"],
-                       inp["w2_sh"], B.cfg_from(cfg), T, overlap=overlap)
+                       inp["w2_sh"], B.cfg_from(cfg), T, overlap=overlap,
+                       fused_combine=fused_combine)
     idx, w = cuda_i32((T, cfg.k)), cuda_f32((T, cfg.k))
     scores, offs = cuda_f32((T, cfg.E)), cuda_i32(cfg.E + 1)
     out = layer.forward(inp["x"], scores_out=scores, topk_idx_out=idx, topk_w_out=w,
@@ -183,3 +184,38 @@ def test_layer_edge_cases(oracle, cfg, forced):
                           abs_margin=tc_router_atol(cfg.d))
     assert (same | amb).all()
     assert_bf16_close(np_(out)[same], rout[same], cfg.name)
+
+
+@pytest.mark.parametrize("cfg", [SMALL_BF16[0], SMALL_BF16[1], EDGE[0][0]], ids=lambda c: c.name)
+def test_layer_fused_combine(oracle, cfg):
+    """The down projection adding its results straight into the output (fp32
+    atomics) agrees with the oracle at the bf16 tolerances, and with the
+    unfused layer to fp32 rounding of a reordered sum."""
+    inp = inputs.make_inputs(cfg, seed=2, device="cuda")
+    out_f, idx, w, scores, offs = run_layer(cfg, inp, fused_combine=True)
+    out_u, *_ = run_layer(cfg, inp, fused_combine=False)
+    assert torch.isfinite(out_f).all()
+    assert rel_fro(np_(out_f), np_(out_u)) < 1e-6
+    sc, ridx, rw, rout = oracle_tokens(oracle, cfg, inp, torch.arange(cfg.T, device="cuda"))
+    same = (np_(idx) == ridx).all(1)
+    assert_bf16_close(np_(out_f)[same], rout[same], cfg.name)
+
+
+def test_layer_fused_combine_full_size_sampled(oracle):
+    cfg = inputs.CONFIGS["dsv3_prefill"]
+    inp = inputs.make_inputs(cfg, seed=0, device="cuda")
+    out, idx, w, scores, offs = run_layer(cfg, inp, fused_combine=True)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    g = torch.Generator()
+    g.manual_seed(9)
+    tok = torch.randperm(cfg.T, generator=g)[:16].sort().values
+    sc, ridx, rw, rout = oracle_tokens(oracle, cfg, inp, tok.cuda())
+    same = (np_(idx[tok.cuda()]) == ridx).all(1)
+    amb = near_tie_tokens(sc, np_(inp["bias"]), cfg.k, cfg.n_group, cfg.topk_group,
+                          abs_margin=tc_router_atol(cfg.d))
+    assert (same | amb).all()
+    assert_bf16_close(np_(out[tok.cuda()])[same], rout[same], cfg.name)
+    del inp, out
+    gc.collect()
+    torch.cuda.empty_cache()
