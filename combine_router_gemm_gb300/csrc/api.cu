@@ -97,17 +97,19 @@ size_t route_ws(int T, int E, int d, int dtype) {
 // `scores`; fp32 activations: fp32 CUDA-core GEMM writing `scores`.
 int run_route(const void* x, int dtype, const float* w_router, const float* bias, int T, int d,
               const moe_route_cfg* cfg, float* scores, int32_t* idx, float* w, void* rws,
-              uint32_t* err, unsigned* work, cudaStream_t s) {
+              uint32_t* err, unsigned* work, cudaStream_t s, cudaEvent_t after_gemm = nullptr) {
     const int E = cfg->num_experts;
     if (dtype == MOE_BF16) {
         float* partial = nullptr;
         int ks = 0;
         int rc = moe_tc::router_bf16(x, w_router, T, d, E, rws, err, work, &partial, &ks, s);
         if (rc != MOE_OK) return rc;
+        if (after_gemm && cudaEventRecord(after_gemm, s) != cudaSuccess) return MOE_ERR_CUDA;
         return moe_launch::topk(nullptr, bias, T, cfg, idx, w, s, partial, ks, scores);
     }
     int rc = moe_launch::router_gemm(x, dtype, w_router, T, d, E, cfg->score_fn, scores, s);
     if (rc != MOE_OK) return rc;
+    if (after_gemm && cudaEventRecord(after_gemm, s) != cudaSuccess) return MOE_ERR_CUDA;
     return moe_launch::topk(scores, bias, T, cfg, idx, w, s);
 }
 
@@ -345,33 +347,44 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
         if (rc == MOE_OK && stage[i] && cudaEventRecord(stage[i], s0) != cudaSuccess) rc = MOE_ERR_CUDA;
     };
     mark(0);
-    // bf16 with a shared expert of the routed experts' size: the shared expert
-    // runs inside the routed grouped-GEMM launches (its compute-bound tiles
-    // interleaved with the weight-streaming ones).  Otherwise it runs as its
-    // own launches, on stream2 when given.
+    // bf16 with a shared expert of the routed experts' size: its down tiles
+    // run inside the routed down launch; its gate/up runs on stream2 (when
+    // given) while the routing and dispatch kernels leave the tensor cores
+    // idle, else inside the routed gate/up launch.  Other shapes: the shared
+    // expert as launches of its own, on stream2 when given.
     const bool merged = sh && a->dtype == MOE_BF16 && a->I_sh == I;
-    moe_tc::SharedExpert shx{a->x, T, a->w13_sh, a->w2_sh, w.hsh, w.ysh};
+    const bool two_streams = s1 && s1 != s0;
+    moe_tc::SharedExpert shx{a->x, T, a->w13_sh, a->w2_sh, w.hsh, w.ysh,
+                             /*in_gate_up=*/!two_streams, /*in_down=*/true};
     cudaEvent_t ev_start = nullptr, ev_shared = nullptr;
-    const bool overlap = sh && !merged && s1 && s1 != s0;
-    if (overlap) {
-        if (cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ev_shared, cudaEventDisableTiming) != cudaSuccess) {
-            if (ev_start) cudaEventDestroy(ev_start);
-            return MOE_ERR_CUDA;
-        }
-        if (cudaEventRecord(ev_start, s0) != cudaSuccess ||
-            cudaStreamWaitEvent(s1, ev_start, 0) != cudaSuccess)
-            rc = MOE_ERR_CUDA;
-        if (rc == MOE_OK)
-            rc = run_ffn(a->x, nullptr, 1, T, d, a->I_sh, a->w13_sh, a->w2_sh, a->dtype, w.ysh, w.hsh,
-                         w.err, ctr(w.err, CTR_SHARED), s1);
-        if (rc == MOE_OK && cudaEventRecord(ev_shared, s1) != cudaSuccess) rc = MOE_ERR_CUDA;
+    const bool overlap = sh && two_streams;
+    if (overlap &&
+        (cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) != cudaSuccess ||
+         cudaEventCreateWithFlags(&ev_shared, cudaEventDisableTiming) != cudaSuccess)) {
+        if (ev_start) cudaEventDestroy(ev_start);
+        return MOE_ERR_CUDA;
     }
+    // the shared expert on stream2 starts once the router GEMM is done: the
+    // router's tiles cannot share an SM with a grouped-GEMM tile, while the
+    // top-k and dispatch kernels can
     if (rc == MOE_OK)
         rc = run_route(a->x, a->dtype, a->w_router, a->bias, T, d, &a->route, w.scores, w.idx, w.w,
-                       w.wsplit, w.err, ctr(w.err, CTR_ROUTER), s0);
+                       w.wsplit, w.err, ctr(w.err, CTR_ROUTER), s0, overlap ? ev_start : nullptr);
     mark(1);
     mark(2);
+    if (overlap) {
+        if (rc == MOE_OK && cudaStreamWaitEvent(s1, ev_start, 0) != cudaSuccess) rc = MOE_ERR_CUDA;
+        if (rc == MOE_OK) {
+            if (merged)  // gate/up only; the down tiles ride in the routed launch
+                rc = moe_tc::grouped_ffn_bf16(a->x, nullptr, 1, T, d, I, a->w13_sh, a->w2_sh, w.ysh,
+                                              w.hsh, w.err, ctr(w.err, CTR_SHARED), s1, nullptr,
+                                              nullptr, nullptr, /*parts=*/1);
+            else
+                rc = run_ffn(a->x, nullptr, 1, T, d, a->I_sh, a->w13_sh, a->w2_sh, a->dtype, w.ysh,
+                             w.hsh, w.err, ctr(w.err, CTR_SHARED), s1);
+        }
+        if (rc == MOE_OK && cudaEventRecord(ev_shared, s1) != cudaSuccess) rc = MOE_ERR_CUDA;
+    }
     const bool fused = a->flags & MOE_LAYER_FUSED_COMBINE;
     if (rc == MOE_OK)
         rc = moe_launch::dispatch(w.idx, a->x, a->dtype, T, d, k, E, w.counts, w.offsets, w.s2r,
@@ -384,7 +397,8 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
         if (merged || fused)
             rc = moe_tc::grouped_ffn_bf16(w.xp, w.offsets, E, T * k, d, I, a->w13, a->w2, w.yp, w.h,
                                           w.err, ctr(w.err, CTR_FFN), s0, stage[4],
-                                          merged ? &shx : nullptr, fused ? &fc : nullptr);
+                                          merged ? &shx : nullptr, fused ? &fc : nullptr, 3,
+                                          merged && overlap ? ev_shared : nullptr);
         else
             rc = run_ffn(w.xp, w.offsets, E, T * k, d, I, a->w13, a->w2, a->dtype, w.yp, w.h,
                          w.err, ctr(w.err, CTR_FFN), s0, stage[4]);
@@ -393,7 +407,7 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     if (rc == MOE_OK && sh && !merged && !overlap)
         rc = run_ffn(a->x, nullptr, 1, T, d, a->I_sh, a->w13_sh, a->w2_sh, a->dtype, w.ysh, w.hsh,
                      w.err, ctr(w.err, CTR_SHARED), s0);
-    if (rc == MOE_OK && overlap && cudaStreamWaitEvent(s0, ev_shared, 0) != cudaSuccess)
+    if (rc == MOE_OK && overlap && !merged && cudaStreamWaitEvent(s0, ev_shared, 0) != cudaSuccess)
         rc = MOE_ERR_CUDA;
     if (rc == MOE_OK && !fused)
         rc = moe_launch::combine(w.yp, w.s2r, w.w, w.ysh, T, k, d, out, w.err, s0);

@@ -68,6 +68,8 @@ struct SharedExpert {
     const void* w2;   // [d,I]
     void* h;          // [T,I] bf16 scratch
     float* y;         // [T,d] fp32 out
+    bool in_gate_up;  // its gate/up tiles ride in the gate/up launch
+    bool in_down;     // its down tiles ride in the down launch (h ready)
 };
 // work: two zeroed counters (gate/up launch, down launch) for the dynamic
 // unit schedule
@@ -78,10 +80,14 @@ struct FusedCombine {
     const int32_t* row_token;  // [rows]
     const float* w_row;        // [rows]
 };
+// parts: 1 = gate/up launch, 2 = down launch, 3 = both.  before_down: an
+// event the down launch waits for (e.g. the shared expert's gate/up on
+// another stream).
 int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
                      const void* w13, const void* w2, float* y, void* h, uint32_t* err,
                      unsigned* work, cudaStream_t s, cudaEvent_t between = nullptr,
-                     const SharedExpert* sh = nullptr, const FusedCombine* fc = nullptr);
+                     const SharedExpert* sh = nullptr, const FusedCombine* fc = nullptr,
+                     int parts = 3, cudaEvent_t before_down = nullptr);
 size_t router_ws_bytes(int T, int E, int d);
 int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s);
 int router_bf16(const void* x, const float* w_router, int T, int d, int E, void* ws,

@@ -840,11 +840,13 @@ namespace moe_tc {
 
 // Both GEMMs of the SwiGLU FFN over bf16 rows; offsets == NULL means one
 // segment [0, rows) with expert 0 (dense).  When sh is given, the shared
-// expert (dense over sh->x, I_sh == I) runs inside the same two launches.
+// expert (dense over sh->x, I_sh == I) runs inside the same launches (those
+// its in_gate_up / in_down flags name).
 int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
                      const void* w13, const void* w2, float* y, void* h, uint32_t* err,
                      unsigned* work, cudaStream_t s, cudaEvent_t between,
-                     const SharedExpert* sh, const FusedCombine* fc) {
+                     const SharedExpert* sh, const FusedCombine* fc, int parts,
+                     cudaEvent_t before_down) {
     if (E > MAX_E) return MOE_ERR_UNSUPPORTED;
     CUtensorMap a1, a2, a1s, a2s;
     BMaps b1, b2, b1s, b2s;
@@ -859,11 +861,12 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     } else {
         a1s = a1; b1s = b1; a2s = a2; b2s = b2;
     }
-    Params p1{offsets, E, rows, d, I, 2 * I, I, h, err, 0, two ? sh->T : 0, two ? sh->h : nullptr,
-              work};
-    Params p2{offsets, E, rows, I, d, d, BM, y, err, 0, two ? sh->T : 0, two ? sh->y : nullptr,
-              work + 1, 1, fc ? fc->out : nullptr, fc ? fc->row_token : nullptr,
-              fc ? fc->w_row : nullptr};
+    const bool two_gu = two && sh->in_gate_up, two_dn = two && sh->in_down;
+    Params p1{offsets, E,   rows, d, I, 2 * I, I, h, err, 0, two_gu ? sh->T : 0,
+              two_gu ? sh->h : nullptr, work};
+    Params p2{offsets, E, rows, I, d, d, BM, y, err, 0, two_dn ? sh->T : 0,
+              two_dn ? sh->y : nullptr, work + 1, 1, fc ? fc->out : nullptr,
+              fc ? fc->row_token : nullptr, fc ? fc->w_row : nullptr};
     // Token tile per launch, from the average rows per expert (the host does
     // not see the device-side offsets).  A 128-row tile leaves room for one
     // more shared-memory stage, so more weight bytes in flight (and, for
@@ -876,9 +879,13 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     //            (prefill: 1.57 ms vs 2.01 ms).
     const bool gu_wide = (long long)rows >= (long long)MOE_GU_WIDE_ROWS * E;
     const bool dn_wide = (long long)rows >= (long long)MOE_DN_WIDE_ROWS * E;
-    int rc = gu_wide ? launch<0, 256>(a1, b1, a1s, b1s, p1, s) : launch<0, 128>(a1, b1, a1s, b1s, p1, s);
+    int rc = MOE_OK;
+    if (parts & 1)
+        rc = gu_wide ? launch<0, 256>(a1, b1, a1s, b1s, p1, s) : launch<0, 128>(a1, b1, a1s, b1s, p1, s);
     if (rc != MOE_OK) return rc;
     if (between && cudaEventRecord(between, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!(parts & 2)) return MOE_OK;
+    if (before_down && cudaStreamWaitEvent(s, before_down, 0) != cudaSuccess) return MOE_ERR_CUDA;
     return dn_wide ? launch<1, 256>(a2, b2, a2s, b2s, p2, s) : launch<1, 128>(a2, b2, a2s, b2s, p2, s);
 }
 

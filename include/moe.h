@@ -207,11 +207,13 @@ typedef struct {
 size_t moe_layer_workspace_size(const moe_layer_args* a);
 
 /* out [T,d] fp32 = the layer: route, dispatch, grouped FFN, shared expert,
- * combine.  With bf16 and I_sh == I the shared expert's tiles run inside the
- * routed grouped-GEMM launches.  Otherwise `stream2` (may be NULL), a second
- * stream of the same device, runs the shared expert concurrently with the
- * routed path, ordered by events; everything is complete on `stream` when
- * the call's work finishes there. */
+ * combine.  `stream2` (may be NULL) is a second stream of the same device.
+ * With bf16 and I_sh == I the shared expert's down tiles run inside the
+ * routed down launch, and its gate/up runs on stream2 (from the end of the
+ * router GEMM, concurrently with top-k and dispatch) or, without stream2,
+ * inside the routed gate/up launch.  Other shapes run the shared expert as
+ * launches of its own, on stream2 when given.  Streams are ordered by events;
+ * everything is complete on `stream` when the call's work finishes there. */
 int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, void* stream,
               void* stream2);
 
