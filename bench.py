@@ -34,14 +34,17 @@ UNIT = "tokens/s"
 L2_FLUSH_BYTES = 512 << 20
 
 
-def launches_per_step(cfg) -> int:
+def launches_per_step(cfg, two_streams: bool) -> int:
     """Our kernels per moe_layer call."""
     n = 5  # top-k, count+scan, permute, combine, router GEMM
     if cfg.dtype == "bf16":
         n += 1  # router weight split
-    n += 2  # gate/up and down grouped GEMMs (routed; the shared expert rides along)
-    if cfg.shared_I and not (cfg.dtype == "bf16" and cfg.shared_I == cfg.I):
-        n += 2  # separate shared-expert launches
+    n += 2  # gate/up and down grouped GEMMs (routed)
+    if cfg.shared_I:
+        if cfg.dtype == "bf16" and cfg.shared_I == cfg.I:
+            n += 1 if two_streams else 0  # shared gate/up on the second stream
+        else:
+            n += 2  # separate shared-expert launches
     return n
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the routed
@@ -50,9 +53,11 @@ def launches_per_step(cfg) -> int:
 # scaled x8 (experts and tokens) and the shared expert's weights are not
 # (profiles/grouped_gemm_tc_dsv3_prefill_e32.md).  Reported as null once the
 # kernel source no longer matches the captured one.
-TRAFFIC = {"source_sha256": "e0ce3365da40382c797e87f921e05ccd296241ae6453082986aae15c6c595162",
-           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 2.087016e9,
-                                            "dsv3_prefill": 8 * (2.087016e9 - 0.0587e9) + 0.0587e9}}
+TRAFFIC = {"source_sha256": "48f5ad945ae7f3983ad163ad822315635422b84cc32fe3387ce02a6027beecd3",
+           # routed gate/up launch (the shared expert's gate/up runs on the
+           # second stream); every term scales with E and the slot count
+           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.963153e9,
+                                            "dsv3_prefill": 8 * 1.963153e9}}
 
 
 def peaks():
@@ -312,11 +317,17 @@ def run_ours(args, cfg):
     gu_flops = 2.0 * S * d * 2 * I
     dn_bytes = active * d * I * es + S * I * es + S * d * 4
     dn_flops = 2.0 * S * I * d
-    merged = cfg.shared_I and cfg.dtype == "bf16" and cfg.shared_I == cfg.I
-    if merged:  # the shared expert's tiles run inside the same two launches
-        Is = cfg.shared_I
+    # bf16, I_sh == I: the shared expert's down tiles run in the routed down
+    # launch; its gate/up tiles in the routed gate/up launch only without a
+    # second stream (with one, they run in a launch of their own)
+    two_streams = layer.stream2 is not None
+    merged = bool(cfg.shared_I) and cfg.dtype == "bf16" and cfg.shared_I == cfg.I
+    merged_gu = merged and not two_streams
+    Is = cfg.shared_I
+    if merged_gu:
         gu_bytes += 2 * Is * d * es + T * d * es + T * Is * es
         gu_flops += 2.0 * T * d * 2 * Is
+    if merged:
         dn_bytes += d * Is * es + T * Is * es + T * d * 4
         dn_flops += 2.0 * T * Is * d
     perm_bytes = T * d * es + S * d * es + S * 4 * 3 + S * 4
@@ -352,7 +363,7 @@ def run_ours(args, cfg):
                 "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
                 "frac": round(tf(gu_flops, ms) / pk["bf16_sustained"], 4)}
     roof.update(traffic=traffic,
-                kernel="grouped_gemm_tc gate/up+SwiGLU (routed" + (" + shared)" if merged else ")"),
+                kernel="grouped_gemm_tc gate/up+SwiGLU (routed" + (" + shared)" if merged_gu else ")"),
                 algorithmic_bytes=gu_bytes, algorithmic_flops=gu_flops,
                 arithmetic_intensity=round(ai, 1), peak_source=pk["source"],
                 launch_ms=round(ms, 4))
@@ -384,7 +395,7 @@ def run_ours(args, cfg):
         cpu = cpu_baseline(cfg, inp)
 
     if rank == 0:
-        launches = launches_per_step(cfg) * K
+        launches = launches_per_step(cfg, two_streams) * K
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": warm, "ms_per_step": 1e3 * total_s / K, "higher_is_better": True,
