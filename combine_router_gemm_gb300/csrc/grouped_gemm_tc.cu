@@ -64,9 +64,10 @@ constexpr int MAX_E = 1024;
 //         accumulator per term (tensor-core accumulation truncates at every
 //         MMA, so the small terms must not share the large term's
 //         accumulator), summed in the epilogue
-// BN is the token tile (MMA N upper bound).  Stages fill ~200 KB of shared
-// memory; accumulators are double-buffered when tensor memory allows.
-constexpr int SMEM_BUDGET = 200 * 1024;
+// BN is the token tile (MMA N upper bound).  Stages fill up to 216 KB of
+// shared memory; accumulators are double-buffered when tensor memory allows.
+constexpr int SMEM_BUDGET = 216 * 1024;
+constexpr int SMEM_LIMIT = 227 * 1024;  // opt-in maximum per CTA
 
 template <int MODE>
 struct ModeCfg;
@@ -77,6 +78,14 @@ struct ModeCfg;
 #endif
 #ifndef MOE_DN_WIDE_ROWS
 #define MOE_DN_WIDE_ROWS 32
+#endif
+// token tile of the gate/up launch below MOE_GU_WIDE_ROWS rows per expert,
+// and of the down launch from MOE_DN_WIDE_ROWS rows per expert
+#ifndef MOE_GU_BN
+#define MOE_GU_BN 160
+#endif
+#ifndef MOE_DN_BN
+#define MOE_DN_BN 256
 #endif
 template <>
 struct ModeCfg<0> {
@@ -101,7 +110,10 @@ struct Cfg {
     static constexpr bool SPLIT_ACC = ModeCfg<MODE>::SPLIT_ACC;
     static constexpr int STAGE_BYTES = NUM_A * A_TILE_BYTES + BN * BK * 2;
     static constexpr int STAGES = SMEM_BUDGET / STAGE_BYTES;
-    static constexpr int ACC_COLS = SPLIT_ACC ? NUM_A * BN : BN;  // TMEM columns per accumulator
+    // TMEM columns between the split accumulators: BN rounded up to 128, so
+    // every accumulator starts on a 128-column boundary
+    static constexpr int ASTRIDE = (BN + 127) / 128 * 128;
+    static constexpr int ACC_COLS = SPLIT_ACC ? NUM_A * ASTRIDE : BN;  // TMEM columns per accumulator
     // output features per unit: the down projection's A tiles are distinct
     // features; gate/up (W1, W3) and the router's weight terms share features
     static constexpr int FEAT = MODE == 1 ? NUM_A * BM : BM;
@@ -109,6 +121,10 @@ struct Cfg {
     // + barriers/tmem slot + schedule table
     static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + sizeof(int) * 2 * (MAX_E + 1);
     static_assert(STAGES >= 2 && ACC_COLS <= TMEM_COLS, "tile does not fit");
+    // token rows are loaded in whole 32-row boxes: a tile that is not a
+    // multiple of 32 rows would let the last box run past its stage
+    static_assert(BN % B_BOX == 0 && BN <= 256, "token tile must be whole boxes");
+    static_assert(SMEM + 64 <= (size_t)SMEM_LIMIT, "shared memory over the per-CTA limit");
 };
 
 // Tensor maps of one activation matrix with token boxes of 32, 64, 128 and
@@ -367,7 +383,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                            const __grid_constant__ BMaps tm_b2, const Params p) {
     using C = Cfg<MODE, BN_>;
     constexpr int STAGES = C::STAGES, NUM_A = C::NUM_A, ACC = C::ACC_STAGES, BN = C::BN;
-    constexpr int ACC_COLS = C::ACC_COLS;
+    constexpr int ACC_COLS = C::ACC_COLS, ASTRIDE = C::ASTRIDE;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -603,7 +619,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t bdesc = smem_desc_sw(bsm + kk * 32);
 #pragma unroll
                         for (int a = 0; a < NUM_A; ++a) {
-                            const uint32_t dst = C::SPLIT_ACC ? d0 + (uint32_t)(a * BN) : d0;
+                            const uint32_t dst = C::SPLIT_ACC ? d0 + (uint32_t)(a * ASTRIDE) : d0;
                             // the first product into an accumulator overwrites it
                             const bool first = kb == kb0 && kk == 0 && (C::SPLIT_ACC || a == 0);
                             mma_bf16(dst, smem_desc_sw(st + a * A_TILE_BYTES + kk * 32), bdesc,
@@ -665,7 +681,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_ld32(tbase + c0, g);
                 if (MODE == 0) {
                     uint32_t up[32];
-                    tmem_ld32(tbase + BN + c0, up);
+                    tmem_ld32(tbase + ASTRIDE + c0, up);
                     tmem_wait_ld();
                     __nv_bfloat16* H = static_cast<__nv_bfloat16*>(out);
 #pragma unroll
@@ -682,8 +698,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 } else if (MODE == 2) {
                     uint32_t mid[32], lo[32];
-                    tmem_ld32(tbase + BN + c0, mid);
-                    tmem_ld32(tbase + 2 * BN + c0, lo);
+                    tmem_ld32(tbase + ASTRIDE + c0, mid);
+                    tmem_ld32(tbase + 2 * ASTRIDE + c0, lo);
                     tmem_wait_ld();
                     float* Y = static_cast<float*>(out);  // this K part's partial logits
 #pragma unroll
@@ -696,7 +712,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 } else {
                     uint32_t g2[32];
-                    tmem_ld32(tbase + BN + c0, g2);
+                    tmem_ld32(tbase + ASTRIDE + c0, g2);
                     tmem_wait_ld();
                     const int n2 = n + BM;  // the second feature tile
                     const bool n2_ok = n2 < p.N_out;
@@ -868,25 +884,29 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
               two_dn ? sh->y : nullptr, work + 1, 1, fc ? fc->out : nullptr,
               fc ? fc->row_token : nullptr, fc ? fc->w_row : nullptr};
     // Token tile per launch, from the average rows per expert (the host does
-    // not see the device-side offsets).  A 128-row tile leaves room for one
-    // more shared-memory stage, so more weight bytes in flight (and, for
-    // gate/up, a double-buffered accumulator); a 256-row tile brings each
-    // weight tile into one SM once for experts of 129-256 rows and halves
-    // the shared-memory traffic per MMA when the GEMM is compute-bound.
-    //   gate/up: 128 below 384 rows per expert (measured: DeepSeek-V3 prefill
-    //            2.67 ms vs 2.85 ms), else 256;
+    // not see the device-side offsets).  A weight-streaming GEMM runs at the
+    // rate (k-blocks in flight per SM) / (load latency), so the tile trades
+    // stages against passes over the weights: every token tile of an expert
+    // is one more pass over its weight tiles (from L2 after the first).
+    //   gate/up: 160 rows below 384 rows per expert (4 stages of 52 KB; one
+    //            pass for experts of up to 160 rows; single-buffered
+    //            accumulator pair), else 256.  Measured on DeepSeek-V3
+    //            prefill: 2.38 ms with 160, 2.45 ms with 128 (4 stages,
+    //            double-buffered), 2.85 ms with 256 (3 stages);
     //   down:    128 only below 32 rows per expert (decode), else 256
-    //            (prefill: 1.57 ms vs 2.01 ms).
+    //            (prefill: 1.57 ms vs 2.01 ms with 128).
     const bool gu_wide = (long long)rows >= (long long)MOE_GU_WIDE_ROWS * E;
     const bool dn_wide = (long long)rows >= (long long)MOE_DN_WIDE_ROWS * E;
     int rc = MOE_OK;
     if (parts & 1)
-        rc = gu_wide ? launch<0, 256>(a1, b1, a1s, b1s, p1, s) : launch<0, 128>(a1, b1, a1s, b1s, p1, s);
+        rc = gu_wide ? launch<0, 256>(a1, b1, a1s, b1s, p1, s)
+                     : launch<0, MOE_GU_BN>(a1, b1, a1s, b1s, p1, s);
     if (rc != MOE_OK) return rc;
     if (between && cudaEventRecord(between, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (!(parts & 2)) return MOE_OK;
     if (before_down && cudaStreamWaitEvent(s, before_down, 0) != cudaSuccess) return MOE_ERR_CUDA;
-    return dn_wide ? launch<1, 256>(a2, b2, a2s, b2s, p2, s) : launch<1, 128>(a2, b2, a2s, b2s, p2, s);
+    return dn_wide ? launch<1, MOE_DN_BN>(a2, b2, a2s, b2s, p2, s)
+                   : launch<1, 128>(a2, b2, a2s, b2s, p2, s);
 }
 
 int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s) {
