@@ -90,8 +90,10 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
                      int parts = 3, cudaEvent_t before_down = nullptr);
 size_t router_ws_bytes(int T, int E, int d);
 int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s);
+// after_split: recorded once the weight split is done, before the GEMM
 int router_bf16(const void* x, const float* w_router, int T, int d, int E, void* ws,
-                uint32_t* err, unsigned* work, float** partial, int* ksplit, cudaStream_t s);
+                uint32_t* err, unsigned* work, float** partial, int* ksplit, cudaStream_t s,
+                cudaEvent_t after_split = nullptr);
 }  // namespace moe_tc
 
 // ---- internal launchers (one per kernel family), used by api.cu -----------

@@ -926,7 +926,8 @@ size_t router_ws_bytes(int T, int E, int d) {
 // terms: K is cut into *ksplit parts (chosen so that the units fill the SMs),
 // part ks written to partial + ks * T * E.  ws: router_ws_bytes(T, E, d).
 int router_bf16(const void* x, const float* w_router, int T, int d, int E, void* ws,
-                uint32_t* err, unsigned* work, float** partial, int* ksplit, cudaStream_t s) {
+                uint32_t* err, unsigned* work, float** partial, int* ksplit, cudaStream_t s,
+                cudaEvent_t after_split) {
     __nv_bfloat16* wsplit = static_cast<__nv_bfloat16*>(ws);
     const size_t split = ((size_t)3 * E * d * 2 + 255) / 256 * 256;
     float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + split);
@@ -935,6 +936,7 @@ int router_bf16(const void* x, const float* w_router, int T, int d, int E, void*
     split_weight_kernel<<<blocks, 256, 0, s>>>(w_router, n, wsplit);
     int rc = moe_host::launch_status();
     if (rc != MOE_OK) return rc;
+    if (after_split && cudaEventRecord(after_split, s) != cudaSuccess) return MOE_ERR_CUDA;
     CUtensorMap a;
     BMaps b;
     if (!make_map(&a, wsplit, 3ull * E, d, BM) || !make_bmaps(&b, x, T, d)) return MOE_ERR_CUDA;
