@@ -97,55 +97,55 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(const XT* __restrict__
 // ---------------------------------------------------------------- top-k
 //
 // One warp per token.  Lane l holds experts e = i*32 + l (i < EPL), so loads
-// are coalesced.  Every choice is a warp-wide argmax over (key, index) that
-// prefers the larger key and, on equal keys, the lower index.
-
-struct Cand {
-    float v;
-    int e;  // -1: none
-};
+// are coalesced.  Every choice prefers the larger key and, on equal keys, the
+// lower index.  Keys are compared as order-preserving unsigned integers, so
+// that a warp-wide maximum is one redux.sync instead of a shuffle butterfly:
+// the largest key first, then the lowest index holding it.
 
 constexpr int FAST_GROUPS = 8;  // group counts up to this take the all-at-once path
+constexpr int TOPK_THREADS = 128;
+constexpr unsigned FULL = 0xffffffffu;
 
-__device__ __forceinline__ Cand better(Cand a, Cand b) {
-    if (b.e < 0) return a;
-    if (a.e < 0) return b;
-    if (b.v > a.v || (b.v == a.v && b.e < a.e)) return b;
-    return a;
+// a < b  <=>  ord_key(a) < ord_key(b) for non-NaN floats, with -0 mapped as
+// +0 (the two compare equal as floats); every result is > 0
+__device__ __forceinline__ uint32_t ord_key(float f) {
+    uint32_t b = __float_as_uint(f);
+    if (b == 0x80000000u) b = 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t u) {
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
 }
 
-__device__ __forceinline__ Cand warp_best(Cand c) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        Cand o;
-        o.v = __shfl_xor_sync(0xffffffffu, c.v, off);
-        o.e = __shfl_xor_sync(0xffffffffu, c.e, off);
-        c = better(c, o);
-    }
-    return c;
+// the two largest of the warp's (v1 >= v2) pairs, as ordered keys: exact
+// top-2 of the multiset of all pairs' values
+__device__ __forceinline__ void warp_top2(uint32_t v1, uint32_t v2, uint32_t& m1, uint32_t& m2) {
+    m1 = __reduce_max_sync(FULL, v1);
+    const unsigned at = __ballot_sync(FULL, v1 == m1);
+    m2 = __popc(at) >= 2 ? m1 : __reduce_max_sync(FULL, v1 == m1 ? v2 : v1);
 }
 
 template <int EPL>
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ scores,
-                                                   const float* __restrict__ bias, int T, int E,
-                                                   int k, int n_group, int topk_group, int sigmoid,
-                                                   float scale, int32_t* __restrict__ idx_out,
-                                                   float* __restrict__ w_out,
-                                                   const float* __restrict__ partial, int ksplit,
-                                                   float* __restrict__ scores_out) {
+__global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(
+    const float* __restrict__ scores, const float* __restrict__ bias, int T, int E, int k,
+    int n_group, int topk_group, int sigmoid, float scale, int32_t* __restrict__ idx_out,
+    float* __restrict__ w_out, const float* __restrict__ partial, int ksplit,
+    float* __restrict__ scores_out) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
-    float sc[EPL], key[EPL];
-    bool ok[EPL];
+    float sc[EPL];
+    uint32_t ko[EPL];  // ordered selection keys
+    uint32_t ok = 0;   // bit i: expert i*32 + lane is still a candidate
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
         const int e = i * 32 + lane;
-        ok[i] = e < E;
+        const bool in = e < E;
+        if (in) ok |= 1u << i;
         if (partial) {
             // scores from the router's K-part partial logits, summed in order
             float v = 0.f;
-            if (ok[i]) {
+            if (in) {
                 v = partial[(size_t)t * E + e];
                 for (int ks = 1; ks < ksplit; ++ks) v += partial[((size_t)ks * T + t) * E + e];
                 if (sigmoid) v = 1.0f / (1.0f + expf(-v));
@@ -153,52 +153,42 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ sco
             }
             sc[i] = v;
         } else {
-            sc[i] = ok[i] ? scores[(size_t)t * E + e] : 0.f;
+            sc[i] = in ? scores[(size_t)t * E + e] : 0.f;
         }
-        key[i] = ok[i] ? (bias ? sc[i] + bias[e] : sc[i]) : 0.f;
+        ko[i] = ord_key(in ? (bias ? sc[i] + bias[e] : sc[i]) : 0.f);
     }
 
     if (n_group > 1) {
         const int gs = E / n_group;
-        int gid[EPL];  // group of each held expert
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) gid[i] = (i * 32 + lane) / gs;
         unsigned keep = 0;
+        const uint32_t NONE = ord_key(-INFINITY);
         if (n_group <= FAST_GROUPS) {
-            // All groups at once: each lane keeps the two largest of its own
-            // keys per group (-inf = none), then a butterfly merges the pairs
-            // across the warp.  Top-2 of a multiset by values only: the merge
-            // (max(a1,b1), max(min(a1,b1), max(a2,b2))) is exact, and every
-            // group has at least two members, so no -inf survives.
-            float g1[FAST_GROUPS], g2[FAST_GROUPS];
+            // every lane's two largest keys per group (-inf = none), then
+            // each group's top-2 over the warp; every group has at least two
+            // members, so no -inf survives
+            uint32_t g1[FAST_GROUPS], g2[FAST_GROUPS];
 #pragma unroll
-            for (int g = 0; g < FAST_GROUPS; ++g) g1[g] = g2[g] = -INFINITY;
+            for (int g = 0; g < FAST_GROUPS; ++g) g1[g] = g2[g] = NONE;
 #pragma unroll
             for (int i = 0; i < EPL; ++i) {
+                const int gi = (i * 32 + lane) / gs;
 #pragma unroll
                 for (int g = 0; g < FAST_GROUPS; ++g) {
-                    if (ok[i] && gid[i] == g) {
-                        const float v = key[i];
-                        g2[g] = fmaxf(g2[g], fminf(g1[g], v));
-                        g1[g] = fmaxf(g1[g], v);
+                    if (((ok >> i) & 1u) && gi == g) {
+                        g2[g] = max(g2[g], min(g1[g], ko[i]));
+                        g1[g] = max(g1[g], ko[i]);
                     }
                 }
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-#pragma unroll
-                for (int g = 0; g < FAST_GROUPS; ++g) {
-                    const float o1 = __shfl_xor_sync(0xffffffffu, g1[g], off);
-                    const float o2 = __shfl_xor_sync(0xffffffffu, g2[g], off);
-                    g2[g] = fmaxf(fminf(g1[g], o1), fmaxf(g2[g], o2));
-                    g1[g] = fmaxf(g1[g], o1);
-                }
-            }
-            // every lane now holds every group score: pick the best groups,
-            // ties to the lower group, without further communication
+            // every lane holds every group score: pick the best groups, ties
+            // to the lower group, without further communication
             float gsc[FAST_GROUPS];
 #pragma unroll
-            for (int g = 0; g < FAST_GROUPS; ++g) gsc[g] = g1[g] + g2[g];
+            for (int g = 0; g < FAST_GROUPS; ++g) {
+                uint32_t m1 = NONE, m2 = NONE;
+                if (g < n_group) warp_top2(g1[g], g2[g], m1, m2);
+                gsc[g] = key_value(m1) + key_value(m2);
+            }
             for (int r = 0; r < topk_group; ++r) {
                 int best = -1;
                 float bv = 0.f;
@@ -212,39 +202,33 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ sco
                 keep |= 1u << best;
             }
         } else {
+            // group g's score lands in lane g
             float my_gscore = 0.f;
             for (int g = 0; g < n_group; ++g) {
-                // two largest keys of group g (values only; their sum is symmetric)
-                float v1 = -INFINITY, v2 = -INFINITY;
+                uint32_t v1 = NONE, v2 = NONE;
 #pragma unroll
                 for (int i = 0; i < EPL; ++i) {
-                    if (ok[i] && gid[i] == g) {
-                        v2 = fmaxf(v2, fminf(v1, key[i]));
-                        v1 = fmaxf(v1, key[i]);
+                    if (((ok >> i) & 1u) && (i * 32 + lane) / gs == g) {
+                        v2 = max(v2, min(v1, ko[i]));
+                        v1 = max(v1, ko[i]);
                     }
                 }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float o1 = __shfl_xor_sync(0xffffffffu, v1, off);
-                    const float o2 = __shfl_xor_sync(0xffffffffu, v2, off);
-                    v2 = fmaxf(fminf(v1, o1), fmaxf(v2, o2));
-                    v1 = fmaxf(v1, o1);
-                }
-                if (lane == g) my_gscore = v1 + v2;
+                uint32_t m1, m2;
+                warp_top2(v1, v2, m1, m2);
+                if (lane == g) my_gscore = key_value(m1) + key_value(m2);
             }
-            bool gtaken = false;
+            // best groups: largest score, ties to the lower group
+            uint32_t gk = lane < n_group ? ord_key(my_gscore) : 0u;
             for (int r = 0; r < topk_group; ++r) {
-                Cand c;
-                c.v = my_gscore;
-                c.e = (lane < n_group && !gtaken) ? lane : -1;
-                c = warp_best(c);
-                if (lane == c.e) gtaken = true;
-                keep |= 1u << c.e;
+                const uint32_t m = __reduce_max_sync(FULL, gk);
+                const int g = (int)__reduce_min_sync(FULL, gk == m ? (uint32_t)lane : FULL);
+                keep |= 1u << g;
+                if (lane == g) gk = 0u;
             }
         }
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
-            if (ok[i] && !((keep >> gid[i]) & 1u)) ok[i] = false;
+            if (!((keep >> ((i * 32 + lane) / gs)) & 1u)) ok &= ~(1u << i);
     }
 
     // softmax normaliser over all E logits
@@ -254,41 +238,44 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ sco
         for (int i = 0; i < EPL; ++i)
             if (i * 32 + lane < E) m = fmaxf(m, sc[i]);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
             if (i * 32 + lane < E) z += expf(sc[i] - m);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(FULL, z, off);
     }
 
     int my_e = 0;
     float my_p = 0.f, psum = 0.f;
     for (int j = 0; j < k; ++j) {
-        Cand c;
-        c.e = -1;
-        c.v = 0.f;
+        // this lane's best candidate: ascending i with strict > keeps the
+        // lowest index among equal keys
+        uint32_t best = 0u;
+        int bi = -1;
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) {  // ascending e: strict > keeps the lowest index
-            if (ok[i] && (c.e < 0 || key[i] > c.v)) {
-                c.v = key[i];
-                c.e = i * 32 + lane;
+        for (int i = 0; i < EPL; ++i) {
+            if (((ok >> i) & 1u) && (bi < 0 || ko[i] > best)) {
+                best = ko[i];
+                bi = i;
             }
         }
-        c = warp_best(c);
+        const uint32_t mk = __reduce_max_sync(FULL, best);
+        const int e = (int)__reduce_min_sync(
+            FULL, (bi >= 0 && best == mk) ? (uint32_t)(bi * 32 + lane) : FULL);
         float s_sel = 0.f;
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
-            if (i * 32 + lane == c.e) {
-                ok[i] = false;
+            if (i * 32 + lane == e) {
+                ok &= ~(1u << i);
                 s_sel = sc[i];
             }
         }
-        s_sel = __shfl_sync(0xffffffffu, s_sel, c.e & 31);
+        s_sel = __shfl_sync(FULL, s_sel, e & 31);
         const float p = sigmoid ? s_sel : expf(s_sel - m) / z;
         psum += p;  // slot order
         if (lane == j) {
-            my_e = c.e;
+            my_e = e;
             my_p = p;
         }
     }
@@ -316,10 +303,10 @@ int router_gemm(const void* x, int dtype, const float* w_router, int T, int d, i
 int topk(const float* scores, const float* bias, int T, const moe_route_cfg* c, int32_t* idx,
          float* w, cudaStream_t s, const float* partial, int ksplit, float* scores_out) {
     const int E = c->num_experts;
-    const int blocks = moe::ceil_div(T, 8);
+    const int blocks = moe::ceil_div(T, TOPK_THREADS / 32);
     const int sig = c->score_fn == MOE_SCORE_SIGMOID;
 #define MOE_TOPK(EPL)                                                                          \
-    topk_kernel<EPL><<<blocks, 256, 0, s>>>(scores, bias, T, E, c->top_k, c->n_group,          \
+    topk_kernel<EPL><<<blocks, TOPK_THREADS, 0, s>>>(scores, bias, T, E, c->top_k, c->n_group, \
                                             c->topk_group, sig, c->routed_scale, idx, w, partial, \
                                             ksplit, scores_out)
     const int epl = moe::ceil_div(E, 32);

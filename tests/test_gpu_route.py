@@ -49,6 +49,26 @@ def test_route_from_scores_bit_exact(oracle, T, E, k, ng, tg, fn, use_bias, qb, 
     np.testing.assert_allclose(np_(w), ref_w, rtol=GATE_RTOL, atol=1e-7)
 
 
+@pytest.mark.parametrize("E,k,ng,tg,fn", [(8, 2, 1, 1, "softmax"), (256, 8, 8, 4, "sigmoid"),
+                                          (64, 6, 16, 3, "sigmoid")])
+def test_route_signed_zero_keys_tie(oracle, E, k, ng, tg, fn):
+    # +0 and -0 compare equal as fp32 keys, so every choice falls to the
+    # lowest index, as it does in the oracle
+    T = 300
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    neg = torch.rand((T, E), generator=g, device="cuda") < 0.5
+    scores = torch.where(neg, torch.tensor(-0.0, device="cuda"), torch.tensor(0.0, device="cuda"))
+    assert torch.signbit(scores).any() and not torch.signbit(scores).all()
+    cfg = B.route_cfg(E, k, ng, tg, B.SIGMOID if fn == "sigmoid" else B.SOFTMAX, 1.0)
+    idx, w = cuda_i32((T, k)), cuda_f32((T, k))
+    B.moe_route_from_scores(scores, None, cfg, idx, w)
+    torch.cuda.synchronize()
+    ref_idx = oracle.select(np_(scores), k, bias=None, n_group=ng, topk_group=tg)
+    np.testing.assert_array_equal(np_(idx), ref_idx)
+    np.testing.assert_array_equal(ref_idx, np.tile(np.arange(k, dtype=ref_idx.dtype), (T, 1)))
+
+
 @pytest.mark.parametrize("name", ["tiny_fp32", "mixtral_bf16", "dsv3_prefill", "dsv3_zipf"])
 def test_route_full_router(oracle, name):
     """moe_route on the workload's own x and router weights: scores close to the
