@@ -53,11 +53,11 @@ def launches_per_step(cfg, two_streams: bool) -> int:
 # scaled x8 (experts and tokens) and the shared expert's weights are not
 # (profiles/grouped_gemm_tc_dsv3_prefill_e32.md).  Reported as null once the
 # kernel source no longer matches the captured one.
-TRAFFIC = {"source_sha256": "48f5ad945ae7f3983ad163ad822315635422b84cc32fe3387ce02a6027beecd3",
+TRAFFIC = {"source_sha256": "f9116c00a50d36d645faf3094b6f1862dfe8965e25d5a4c5995c167bc2fc7157",
            # routed gate/up launch (the shared expert's gate/up runs on the
            # second stream); every term scales with E and the slot count
-           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.963153e9,
-                                            "dsv3_prefill": 8 * 1.963153e9}}
+           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.960612e9,
+                                            "dsv3_prefill": 8 * 1.960612e9}}
 
 
 def peaks():
