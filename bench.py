@@ -188,6 +188,92 @@ def host_weights(inp):
     return {k: npy(inp[k]) for k in ("w13", "w2", "w_router", "bias", "w13_sh", "w2_sh")}
 
 
+def eager_layer(cfg, inp):
+    """The same layer as plain PyTorch GPU ops (a comparator, timed only):
+    fp32 router, torch.topk selection, one matmul chain per active expert,
+    index_add_ combine."""
+    import torch
+    import torch.nn.functional as F
+    x, T, E, k, I = inp["x"], cfg.T, cfg.E, cfg.k, cfg.I
+    logits = x.float() @ inp["w_router"].t()
+    if cfg.score_fn == "sigmoid":
+        s = torch.sigmoid(logits)
+        key = s + inp["bias"] if inp["bias"] is not None else s
+    else:
+        s = logits
+        key = logits
+    if cfg.n_group > 1:
+        gs = key.view(T, cfg.n_group, E // cfg.n_group).topk(2, dim=-1).values.sum(-1)
+        keep = torch.zeros_like(gs, dtype=torch.bool)
+        keep.scatter_(1, gs.topk(cfg.topk_group, dim=-1).indices, True)
+        key = key.masked_fill(~keep.repeat_interleave(E // cfg.n_group, dim=1), float("-inf"))
+    idx = key.topk(k, dim=-1).indices
+    if cfg.score_fn == "sigmoid":
+        w = s.gather(1, idx)
+    else:
+        w = torch.softmax(logits, dim=-1).gather(1, idx)
+    w = w / w.sum(-1, keepdim=True) * cfg.routed_scale
+    flat = idx.reshape(-1)
+    order = torch.argsort(flat, stable=True)
+    counts = torch.bincount(flat, minlength=E).tolist()
+    tok = order // k
+    wsel = w.reshape(-1)[order]
+    out = torch.zeros((T, cfg.d), dtype=torch.float32, device=x.device)
+    start = 0
+    for e, n in enumerate(counts):
+        if n == 0:
+            continue
+        rows = tok[start:start + n]
+        xe = x[rows]
+        gu = xe @ inp["w13"][e].t()
+        h = (F.silu(gu[:, :I].float()) * gu[:, I:].float()).to(x.dtype)
+        y = (h @ inp["w2"][e].t()).float()
+        out.index_add_(0, rows, y * wsel[start:start + n, None])
+        start += n
+    if inp["w13_sh"] is not None:
+        gu = x @ inp["w13_sh"].t()
+        Is = cfg.shared_I
+        h = (F.silu(gu[:, :Is].float()) * gu[:, Is:].float()).to(x.dtype)
+        out += (h @ inp["w2_sh"].t()).float()
+    return out
+
+
+def time_cuda(fn, steps, flush):
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    return statistics.median(ms)
+
+
+def comparators(cfg, inp, ours_out, flush, steps=3):
+    """PyTorch comparator on the same inputs: the eager layer.  Reports what
+    it measured, or why it could not run.  (A library grouped GEMM,
+    torch._grouped_mm of torch 2.9.1, failed with an unspecified launch
+    failure on GB300 and is not run.)"""
+    import torch
+    res = {}
+    if cfg.dtype != "bf16":
+        return res
+    try:
+        ms = time_cuda(lambda: eager_layer(cfg, inp), steps, flush)
+        ref = eager_layer(cfg, inp)
+        rel = float(torch.linalg.norm(ref - ours_out) / torch.linalg.norm(ref))
+        res["torch_eager_layer"] = {"ms": round(ms, 3), "tokens_per_s": round(cfg.T / ms * 1e3, 1),
+                                    "rel_fro_vs_ours": rel}
+    except Exception as exc:  # a comparator that cannot run is reported, not fatal
+        res["torch_eager_layer"] = {"unavailable": f"{type(exc).__name__}: {exc}"[:200]}
+    return res
+
+
 def cpu_baseline(cfg, inp, target_s=15.0):
     import oracle
     inp["_host"] = inp.get("_host") or host_weights(inp)
@@ -390,6 +476,12 @@ def run_ours(args, cfg):
                "d2h_bytes_per_step": T * d * 4, "steps": ne,
                "pipelined": "H2D of step i+1 and D2H of step i-1 overlap step i"}
 
+    comp = None
+    if rank == 0 and world == 1 and not args.no_comparators:
+        layer.forward(x, out=out)
+        torch.cuda.synchronize()
+        comp = comparators(cfg, inp, out, flush)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg, inp)
@@ -404,6 +496,8 @@ def run_ours(args, cfg):
             "gpu_launches": launches, "clocks": clk.summary(), "stages": stages,
             "active_experts": active, "wall_s_timed": round(t_wall, 3),
         }
+        if comp:
+            line["comparators"] = comp
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -420,6 +514,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-comparators", action="store_true",
+                    help="skip the PyTorch comparator (the eager layer)")
     ap.add_argument("--no-overlap", action="store_true", help="shared expert on the main stream")
     ap.add_argument("--fused-combine", action="store_true",
                     help="add the down projection's results straight into the output (atomics)")
