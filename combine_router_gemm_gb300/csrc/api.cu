@@ -379,8 +379,16 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
                        w.wsplit, w.err, ctr(w.err, CTR_ROUTER), s0, overlap ? ev_start : nullptr);
     mark(1);
     mark(2);
+    const bool fused = a->flags & MOE_LAYER_FUSED_COMBINE;
+    // fused combine: the output is accumulated into, so it starts at zero;
+    // on stream2 (before the shared expert, which the down launch waits for)
+    // when given, so that the main stream does not pay for it
+    const bool zero_on_s1 = fused && merged && overlap;
     if (overlap) {
         if (rc == MOE_OK && cudaStreamWaitEvent(s1, ev_start, 0) != cudaSuccess) rc = MOE_ERR_CUDA;
+        if (rc == MOE_OK && zero_on_s1 &&
+            cudaMemsetAsync(out, 0, sizeof(float) * (size_t)T * d, s1) != cudaSuccess)
+            rc = MOE_ERR_CUDA;
         if (rc == MOE_OK) {
             if (merged)  // gate/up only; the down tiles ride in the routed launch
                 rc = moe_tc::grouped_ffn_bf16(a->x, nullptr, 1, T, d, I, a->w13_sh, a->w2_sh, w.ysh,
@@ -392,12 +400,12 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
         }
         if (rc == MOE_OK && cudaEventRecord(ev_shared, s1) != cudaSuccess) rc = MOE_ERR_CUDA;
     }
-    const bool fused = a->flags & MOE_LAYER_FUSED_COMBINE;
     if (rc == MOE_OK)
         rc = moe_launch::dispatch(w.idx, a->x, a->dtype, T, d, k, E, w.counts, w.offsets, w.s2r,
                                   w.r2t, w.xp, w.disp, w.err, s0, fused ? w.w : nullptr, w.w_row);
     mark(3);
-    if (rc == MOE_OK && fused && cudaMemsetAsync(out, 0, sizeof(float) * (size_t)T * d, s0) != cudaSuccess)
+    if (rc == MOE_OK && fused && !zero_on_s1 &&
+        cudaMemsetAsync(out, 0, sizeof(float) * (size_t)T * d, s0) != cudaSuccess)
         rc = MOE_ERR_CUDA;
     const moe_tc::FusedCombine fc{out, w.r2t, w.w_row};
     if (rc == MOE_OK) {

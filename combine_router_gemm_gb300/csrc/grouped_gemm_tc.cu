@@ -282,6 +282,19 @@ __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// element i (0..3, run-time) of four values, by selects (no local memory)
+__device__ __forceinline__ float pick4(const float (&a)[4], int i) {
+    const float lo = (i & 1) ? a[1] : a[0];
+    const float hi = (i & 1) ? a[3] : a[2];
+    return (i & 2) ? hi : lo;
+}
+// accumulator value j0 + i (i run-time, 0..3) of a tcgen05.ld result, as float
+__device__ __forceinline__ float sel4(const uint32_t (&g)[32], int j0, int i) {
+    const float a[4] = {__uint_as_float(g[j0]), __uint_as_float(g[j0 + 1]),
+                        __uint_as_float(g[j0 + 2]), __uint_as_float(g[j0 + 3])};
+    return pick4(a, i);
+}
+
 // ---------------------------------------------------------------- schedule
 
 struct Unit {
@@ -717,17 +730,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int n2 = n + BM;  // the second feature tile
                     const bool n2_ok = n2 < p.N_out;
                     if (p.comb_out) {
-                        // fused combine: weighted adds into the token's output row
+                        // fused combine: weighted adds into the token's output
+                        // row.  A 4x4 transpose inside each group of four lanes
+                        // gives every lane four consecutive features of one
+                        // token, added with one 16-byte vector reduction.
+                        const int b = lane & 3;
+                        const int nq = n - b;  // the quad's first feature
+                        const bool q_ok = nq < p.N_out, q2_ok = nq + BM < p.N_out;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int tok = c0 + j;
+                        for (int j0 = 0; j0 < 32; j0 += 4) {
+                            float r1[4], r2[4];  // r1[k]: feature nq + ((b + k) & 3)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                // lane b sends its token j0 + ((b - k) & 3) and
+                                // receives feature (b + k) & 3 of token j0 + b
+                                const int snd = (b - k) & 3;
+                                const int src = (lane & ~3) | ((b + k) & 3);
+                                const float v1 = sel4(g, j0, snd), v2 = sel4(g2, j0, snd);
+                                r1[k] = k == 0 ? v1 : __shfl_sync(0xffffffffu, v1, src);
+                                r2[k] = k == 0 ? v2 : __shfl_sync(0xffffffffu, v2, src);
+                            }
+                            const int tok = c0 + j0 + b;
                             if (tok < t.n_tok) {
                                 const int r = t.m_start + tok;
                                 const int tk = t.second ? r : p.row_token[r];
                                 const float wgt = t.second ? 1.0f : p.w_row[r];
-                                float* row = p.comb_out + (size_t)tk * p.N_out;
-                                if (n_ok) atomicAdd(row + n, wgt * __uint_as_float(g[j]));
-                                if (n2_ok) atomicAdd(row + n2, wgt * __uint_as_float(g2[j]));
+                                float* row = p.comb_out + (size_t)tk * p.N_out + nq;
+                                if (q_ok)
+                                    atomicAdd(reinterpret_cast<float4*>(row),
+                                              make_float4(wgt * pick4(r1, (0 - b) & 3),
+                                                          wgt * pick4(r1, (1 - b) & 3),
+                                                          wgt * pick4(r1, (2 - b) & 3),
+                                                          wgt * pick4(r1, (3 - b) & 3)));
+                                if (q2_ok)
+                                    atomicAdd(reinterpret_cast<float4*>(row + BM),
+                                              make_float4(wgt * pick4(r2, (0 - b) & 3),
+                                                          wgt * pick4(r2, (1 - b) & 3),
+                                                          wgt * pick4(r2, (2 - b) & 3),
+                                                          wgt * pick4(r2, (3 - b) & 3)));
                             }
                         }
                     } else {
