@@ -11,8 +11,10 @@
  *
  * Conventions for every entry point
  *   - Every array argument is a DEVICE pointer unless stated otherwise; the
- *     caller allocates and owns all of them.  The library never allocates,
- *     frees or keeps memory between calls and holds no global state.
+ *     caller allocates and owns all of them.  The library never allocates or
+ *     frees memory.  Between calls it keeps only per-device launch settings
+ *     (the grouped-GEMM kernels' shared-memory limit) and, for
+ *     moe_dispatch_noalloc alone, a fixed scratch array described there.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Work is enqueued asynchronously; nothing synchronises.
  *   - Return value: a moe_status.  Invalid arguments are detected on the host
