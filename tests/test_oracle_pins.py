@@ -398,3 +398,41 @@ def test_zipf_workload_routing_shape(oracle):
     zero = (inputs.to_numpy(inp["bias"]) < -1e3)
     assert zero.sum() == 32 and (counts[zero] == 0).all()
     assert counts.max() > 8 * counts.mean()
+
+
+# ---------------------------------------------------------------- worked examples
+# Hand-derived values (tests/golden/worked_examples.json): each fixture carries
+# the derivation of its expected numbers from the definitions.
+
+GOLDEN = __import__("os").path.join(__import__("os").path.dirname(__file__), "golden",
+                                    "worked_examples.json")
+
+
+def _golden():
+    import json
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("i", range(3))
+def test_worked_routing_examples(oracle, i):
+    ex = _golden()["routing"][i]
+    sc = np.asarray([ex["scores"]], np.float32)
+    bias = None if ex["bias"] is None else np.asarray(ex["bias"], np.float32)
+    idx = oracle.select(sc, ex["k"], bias=bias, n_group=ex["n_group"], topk_group=ex["topk_group"])
+    assert list(idx[0]) == ex["expect_idx"], ex["name"]
+    fn = oracle.SIGMOID if ex["score_fn"] == "sigmoid" else oracle.SOFTMAX
+    w = oracle.gates(sc, idx, fn, ex["routed_scale"])
+    np.testing.assert_allclose(w[0], ex["expect_w"], rtol=1e-6, err_msg=ex["name"])
+
+
+def test_worked_expert_example(oracle):
+    ex = _golden()["expert"][0]
+    x = np.asarray([ex["x"]], np.float32)
+    w13 = np.asarray([ex["w13"]], np.float32)
+    w2 = np.asarray([ex["w2"]], np.float32)
+    sel = np.zeros(1, np.int32)
+    y = oracle.expert_rows(x, sel, w13, w2, round_h=False)
+    np.testing.assert_allclose(y[0], ex["expect_y"], rtol=1e-12)
+    yb = oracle.expert_rows(x, sel, w13, w2, round_h=True)
+    np.testing.assert_array_equal(yb[0], ex["expect_y_bf16_h"])
