@@ -83,3 +83,28 @@ def test_reference_arm_json_line_tiny():
     assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
     assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["e2e"]["d2h_bytes_per_step"] == 0
     assert j["steps"] == 2 and j["higher_is_better"] is True
+
+
+@pytest.mark.parametrize("sigmoid", [False, True])
+def test_eager_comparator_computes_the_layer(oracle, sigmoid):
+    """The bench's PyTorch comparator computes the same layer as the oracle
+    (run here on CPU tensors; it rounds g and u to bf16 where the oracle
+    keeps them in fp32, hence the looser tolerance)."""
+    import numpy as np
+    from combine_router_gemm_gb300 import inputs
+    if sigmoid:
+        cfg = inputs.MoEConfig("t", T=48, d=64, E=16, k=4, I=32, score_fn="sigmoid", n_group=4,
+                               topk_group=2, routed_scale=2.5, shared_I=32, bias="normal")
+    else:
+        cfg = inputs.MoEConfig("m", T=48, d=64, E=8, k=2, I=48)
+    inp = inputs.make_inputs(cfg, seed=0, device="cpu")
+    out = bench.eager_layer(cfg, inp).numpy().astype(np.float64)
+    n = inputs.to_numpy
+    opt = lambda key: None if inp[key] is None else n(inp[key])
+    _, _, ref = oracle.moe_tokens(n(inp["x"]), E=cfg.E, k=cfg.k, w13=n(inp["w13"]), w2=n(inp["w2"]),
+                                  w_router=n(inp["w_router"]), bias=opt("bias"),
+                                  n_group=cfg.n_group, topk_group=cfg.topk_group,
+                                  score_fn=oracle.SIGMOID if sigmoid else oracle.SOFTMAX,
+                                  routed_scale=cfg.routed_scale, w13_sh=opt("w13_sh"),
+                                  w2_sh=opt("w2_sh"), round_h=True)
+    assert np.linalg.norm(out - ref) / np.linalg.norm(ref) < 1e-2
