@@ -186,7 +186,14 @@ def test_layer_edge_cases(oracle, cfg, forced):
     assert_bf16_close(np_(out)[same], rout[same], cfg.name)
 
 
-@pytest.mark.parametrize("cfg", [SMALL_BF16[0], SMALL_BF16[1], EDGE[0][0]], ids=lambda c: c.name)
+# d and I not multiples of 128: partial feature tiles in the fused epilogue
+FUSED_RAGGED = inputs.MoEConfig("fused_ragged", T=333, d=200, E=12, k=3, I=136, dtype="bf16",
+                                score_fn="sigmoid", n_group=1, topk_group=1, routed_scale=1.5,
+                                shared_I=136, bias="normal", expert_std=0.06, router_std=0.06)
+
+
+@pytest.mark.parametrize("cfg", [SMALL_BF16[0], SMALL_BF16[1], EDGE[0][0], FUSED_RAGGED],
+                         ids=lambda c: c.name)
 def test_layer_fused_combine(oracle, cfg):
     """The down projection adding its results straight into the output (fp32
     atomics) agrees with the oracle at the bf16 tolerances, and with the
