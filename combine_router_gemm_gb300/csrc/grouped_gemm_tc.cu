@@ -12,19 +12,19 @@
 //
 // Design (sm_103a):
 //  * Swap-AB: the MMA's M side (128) walks output features (weight rows), its
-//    N side walks tokens (16..256, rounded up to 16 per tile).  Small and
+//    N side walks tokens (16..BN, rounded up to 16 per tile).  Small and
 //    ragged segments then cost N granularity 16 rather than a 128-row tile,
-//    and every weight tile of an expert is read once per 256 tokens.
+//    and every weight tile of an expert is read once per BN tokens.
 //  * One CTA per SM (persistent), 10 warps: warp 0 issues TMA loads, warp 1
 //    allocates tensor memory and issues tcgen05.mma from one thread, warps 2-9
 //    drain the accumulators (tcgen05.ld; two warps per 32-lane quarter) and
-//    store.  Shared-memory stages are
-//    handed over with mbarriers; the accumulator is handed over with a
-//    full/empty mbarrier pair (double-buffered in the down GEMM).
+//    store.  Shared-memory stages are handed over with mbarriers; the
+//    accumulator is handed over with a full/empty mbarrier pair
+//    (double-buffered when tensor memory holds two).
 //  * Operands are K-major bf16 tiles of 64 elements (128 B) per row, loaded by
 //    TMA with the 128-byte swizzle that the tcgen05 shared-memory descriptor
-//    expects; the token tile is loaded in 32-row boxes, only as many as the
-//    segment needs.  Rows past a segment belong to the next expert (or are
+//    expects; the token tile is loaded in at most four boxes of 256/128/64/32
+//    rows, only as many rows (in whole 32-row boxes) as the segment needs.  Rows past a segment belong to the next expert (or are
 //    zero-filled past the matrix); their results are computed and dropped.
 //  * Tiles are enumerated expert-major, feature-tile next, token-tile last, so
 //    CTAs that run at the same time share weight tiles and token tiles in L2.
@@ -897,7 +897,8 @@ namespace moe_tc {
 // Both GEMMs of the SwiGLU FFN over bf16 rows; offsets == NULL means one
 // segment [0, rows) with expert 0 (dense).  When sh is given, the shared
 // expert (dense over sh->x, I_sh == I) runs inside the same launches (those
-// its in_gate_up / in_down flags name).
+// its in_gate_up / in_down flags name).  When fc is given, the down launch
+// adds its results into fc->out instead of writing y.
 int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
                      const void* w13, const void* w2, float* y, void* h, uint32_t* err,
                      unsigned* work, cudaStream_t s, cudaEvent_t between,

@@ -196,8 +196,8 @@ typedef struct {
 } moe_layer_args;
 
 /* moe_layer_args.flags: add the down projection's results straight into `out`
- * (fp32 atomic adds in the grouped GEMM's epilogue) instead of writing the
- * permuted fp32 rows and combining them in a separate pass.  bf16 with the
+ * (16-byte fp32 vector reductions in the grouped GEMM's epilogue) instead of
+ * writing the permuted fp32 rows and combining them in a separate pass.  bf16 with the
  * shared expert of the routed experts' size (or none) only.  The summation
  * order then varies from run to run (results agree to fp32 rounding). */
 #define MOE_LAYER_FUSED_COMBINE 1
@@ -211,8 +211,8 @@ size_t moe_layer_workspace_size(const moe_layer_args* a);
 /* out [T,d] fp32 = the layer: route, dispatch, grouped FFN, shared expert,
  * combine.  `stream2` (may be NULL) is a second stream of the same device.
  * With bf16 and I_sh == I the shared expert's down tiles run inside the
- * routed down launch, and its gate/up runs on stream2 (from the end of the
- * router GEMM, concurrently with top-k and dispatch) or, without stream2,
+ * routed down launch, and its gate/up runs on stream2 (launched with the
+ * router GEMM, concurrently with it, top-k and dispatch) or, without stream2,
  * inside the routed gate/up launch.  Other shapes run the shared expert as
  * launches of its own, on stream2 when given.  Streams are ordered by events;
  * everything is complete on `stream` when the call's work finishes there. */
