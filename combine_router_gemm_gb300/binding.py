@@ -354,6 +354,30 @@ class MoELayer:
         moe_layer(self._args(x, **outs), out, self.ws, stream=stream, stream2=self.stream2)
         return out
 
+    def capture(self, x, out=None, **outs):
+        """Record one ``forward(x)`` into a CUDA graph and return ``(graph,
+        out)``.
+
+        ``graph.replay()`` recomputes the layer from the current contents of
+        the static buffer ``x`` (copy new tokens into it) into the static
+        ``out``; the optional outputs (``scores_out`` ...) are static as well.
+        One call runs first, outside the capture, so that the per-device
+        kernel settings are made before capturing.  The second stream of the
+        layer is forked from and joined back into the capture by events.
+        """
+        if out is None:
+            out = torch.empty((x.shape[0], x.shape[1]), dtype=torch.float32, device=x.device)
+        dev = x.device
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            self.forward(x, out=out, **outs)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+            self.forward(x, out=out, **outs)
+        return graph, out
+
     def forward_host(self, host_inputs, host_outputs):
         """Run the layer over a sequence of host batches, pipelined.
 

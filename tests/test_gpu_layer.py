@@ -226,3 +226,35 @@ def test_layer_fused_combine_full_size_sampled(oracle):
     del inp, out
     gc.collect()
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("cfg", [SMALL_BF16[0], SMALL_BF16[2], inputs.CONFIGS["tiny_fp32"]],
+                         ids=lambda c: c.name)
+def test_layer_cuda_graph_replay(oracle, cfg):
+    """The layer recorded into a CUDA graph (both streams) and replayed on new
+    tokens gives exactly what a direct call gives, and matches the oracle."""
+    inp = inputs.make_inputs(cfg, seed=4, device="cuda")
+    layer = B.MoELayer(inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"],
+                       inp["w2_sh"], B.cfg_from(cfg), cfg.T)
+    x = inp["x"].clone()
+    graph, out = layer.capture(x)
+    for seed in (5, 6):
+        xn = inputs.make_inputs(cfg, seed=seed, device="cuda", experts=False)["x"]
+        x.copy_(xn)
+        graph.replay()
+        direct = layer.forward(xn)
+        torch.cuda.synchronize()
+        assert torch.equal(out, direct)
+    rc, detail = B.moe_check_error(layer.ws)
+    assert rc == B.OK, detail
+    # the last replay's tokens against the oracle
+    inp["x"] = xn
+    tok = torch.arange(cfg.T, device="cuda")
+    sc, ridx, rw, rout = oracle_tokens(oracle, cfg, inp, tok)
+    if cfg.dtype == "f32":
+        assert rel_fro(np_(out), rout) < 1e-5
+    else:
+        idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device="cuda")
+        layer.forward(xn, topk_idx_out=idx)
+        same = (np_(idx) == ridx).all(1)
+        assert_bf16_close(np_(out)[same], rout[same], cfg.name)
