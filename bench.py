@@ -53,11 +53,12 @@ def launches_per_step(cfg, two_streams: bool) -> int:
 # scaled x8 (experts and tokens) and the shared expert's weights are not
 # (profiles/grouped_gemm_tc_dsv3_prefill_e32.md).  Reported as null once the
 # kernel source no longer matches the captured one.
-TRAFFIC = {"source_sha256": "f9116c00a50d36d645faf3094b6f1862dfe8965e25d5a4c5995c167bc2fc7157",
+TRAFFIC = {"source_sha256": "95e685d0a248fa5dc73834f1498701a5ae9d1e6df9bd26a437a190defa539b54",
            # routed gate/up launch (the shared expert's gate/up runs on the
-           # second stream); every term scales with E and the slot count
-           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.960612e9,
-                                            "dsv3_prefill": 8 * 1.960612e9}}
+           # second stream): dsv3_prefill from a one-pass capture of the full
+           # layer, dsv3_prefill_e32 from a capture of the 32-expert case
+           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.960355e9,
+                                            "dsv3_prefill": 15.886749e9}}
 
 
 def peaks():
