@@ -870,9 +870,18 @@ bool make_bmaps(BMaps* m, const void* base, uint64_t rows, uint64_t cols) {
     return true;
 }
 
+#ifndef MOE_BALANCED_GRID
+#define MOE_BALANCED_GRID 1
+#endif
+
+// units: the launch's work units when the host knows them (dense problems,
+// the router), else 0.  With a known count the grid is the smallest one that
+// still needs the same number of waves (256 equal units: 128 CTAs in two
+// waves rather than 152 CTAs in 1.7), which leaves the other SMs to kernels
+// on other streams at no cost to this launch.
 template <int MODE, int BN>
 int launch(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, const BMaps& b2,
-           const Params& p, cudaStream_t s) {
+           const Params& p, cudaStream_t s, long long units = 0) {
     // the shared-memory limit is a per-device attribute of the kernel: set it
     // once per device (setting it twice is harmless, so no lock is needed)
     static bool attr_done[64] = {};
@@ -886,7 +895,13 @@ int launch(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, const BM
             return MOE_ERR_CUDA;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
-    grouped_gemm_tc_kernel<MODE, BN><<<moe_host::num_sms(), NUM_THREADS, smem, s>>>(a, b, a2, b2, p);
+    const int sms = moe_host::num_sms();
+    int grid = sms;
+    if (MOE_BALANCED_GRID && units > 0) {
+        const long long waves = (units + sms - 1) / sms;
+        grid = (int)((units + waves - 1) / waves);
+    }
+    grouped_gemm_tc_kernel<MODE, BN><<<grid, NUM_THREADS, smem, s>>>(a, b, a2, b2, p);
     return moe_host::launch_status();
 }
 
@@ -938,16 +953,24 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     //            (prefill: 1.57 ms vs 2.01 ms with 128).
     const bool gu_wide = (long long)rows >= (long long)MOE_GU_WIDE_ROWS * E;
     const bool dn_wide = (long long)rows >= (long long)MOE_DN_WIDE_ROWS * E;
+    // a dense problem alone (offsets == NULL, no second problem): the unit
+    // counts are known here
+    const bool dense = offsets == nullptr;
+    const int gu_bn = gu_wide ? 256 : MOE_GU_BN, dn_bn = dn_wide ? MOE_DN_BN : 128;
+    const long long gu_units =
+        dense && !two_gu ? (long long)((rows + gu_bn - 1) / gu_bn) * ((I + BM - 1) / BM) : 0;
+    const long long dn_units =
+        dense && !two_dn ? (long long)((rows + dn_bn - 1) / dn_bn) * ((d + 2 * BM - 1) / (2 * BM)) : 0;
     int rc = MOE_OK;
     if (parts & 1)
-        rc = gu_wide ? launch<0, 256>(a1, b1, a1s, b1s, p1, s)
-                     : launch<0, MOE_GU_BN>(a1, b1, a1s, b1s, p1, s);
+        rc = gu_wide ? launch<0, 256>(a1, b1, a1s, b1s, p1, s, gu_units)
+                     : launch<0, MOE_GU_BN>(a1, b1, a1s, b1s, p1, s, gu_units);
     if (rc != MOE_OK) return rc;
     if (between && cudaEventRecord(between, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (!(parts & 2)) return MOE_OK;
     if (before_down && cudaStreamWaitEvent(s, before_down, 0) != cudaSuccess) return MOE_ERR_CUDA;
-    return dn_wide ? launch<1, MOE_DN_BN>(a2, b2, a2s, b2s, p2, s)
-                   : launch<1, 128>(a2, b2, a2s, b2s, p2, s);
+    return dn_wide ? launch<1, MOE_DN_BN>(a2, b2, a2s, b2s, p2, s, dn_units)
+                   : launch<1, 128>(a2, b2, a2s, b2s, p2, s, dn_units);
 }
 
 int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s) {
@@ -989,7 +1012,7 @@ int router_bf16(const void* x, const float* w_router, int T, int d, int E, void*
     Params p{nullptr, 1, T, d, E, 0, E, part, err, 0, 0, nullptr, work, ks};
     *partial = part;
     *ksplit = ks;
-    return launch<2, RBN>(a, b, a, b, p, s);
+    return launch<2, RBN>(a, b, a, b, p, s, (long long)units * ks);
 }
 
 }  // namespace moe_tc
