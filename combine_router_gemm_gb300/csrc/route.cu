@@ -125,7 +125,9 @@ __device__ __forceinline__ void warp_top2(uint32_t v1, uint32_t v2, uint32_t& m1
     m2 = __popc(at) >= 2 ? m1 : __reduce_max_sync(FULL, v1 == m1 ? v2 : v1);
 }
 
-template <int EPL>
+// G32: groups of exactly 32 experts, one per lane and register slot (the
+// group of held expert i is i), e.g. DeepSeek-V3's 8 groups of 32.
+template <int EPL, bool G32>
 __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(
     const float* __restrict__ scores, const float* __restrict__ bias, int T, int E, int k,
     int n_group, int topk_group, int sigmoid, float scale, int32_t* __restrict__ idx_out,
@@ -160,23 +162,31 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(
 
     if (n_group > 1) {
         const int gs = E / n_group;
+        int gid[EPL];  // group of each held expert
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) gid[i] = G32 ? i : (i * 32 + lane) / gs;
         unsigned keep = 0;
         const uint32_t NONE = ord_key(-INFINITY);
-        if (n_group <= FAST_GROUPS) {
+        if (G32 || n_group <= FAST_GROUPS) {
             // every lane's two largest keys per group (-inf = none), then
             // each group's top-2 over the warp; every group has at least two
             // members, so no -inf survives
             uint32_t g1[FAST_GROUPS], g2[FAST_GROUPS];
 #pragma unroll
             for (int g = 0; g < FAST_GROUPS; ++g) g1[g] = g2[g] = NONE;
+            if (G32) {
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) {
-                const int gi = (i * 32 + lane) / gs;
+                for (int i = 0; i < EPL && i < FAST_GROUPS; ++i)
+                    if ((ok >> i) & 1u) g1[i] = ko[i];
+            } else {
 #pragma unroll
-                for (int g = 0; g < FAST_GROUPS; ++g) {
-                    if (((ok >> i) & 1u) && gi == g) {
-                        g2[g] = max(g2[g], min(g1[g], ko[i]));
-                        g1[g] = max(g1[g], ko[i]);
+                for (int i = 0; i < EPL; ++i) {
+#pragma unroll
+                    for (int g = 0; g < FAST_GROUPS; ++g) {
+                        if (((ok >> i) & 1u) && gid[i] == g) {
+                            g2[g] = max(g2[g], min(g1[g], ko[i]));
+                            g1[g] = max(g1[g], ko[i]);
+                        }
                     }
                 }
             }
@@ -208,7 +218,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(
                 uint32_t v1 = NONE, v2 = NONE;
 #pragma unroll
                 for (int i = 0; i < EPL; ++i) {
-                    if (((ok >> i) & 1u) && (i * 32 + lane) / gs == g) {
+                    if (((ok >> i) & 1u) && gid[i] == g) {
                         v2 = max(v2, min(v1, ko[i]));
                         v1 = max(v1, ko[i]);
                     }
@@ -228,7 +238,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(
         }
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
-            if (!((keep >> ((i * 32 + lane) / gs)) & 1u)) ok &= ~(1u << i);
+            if (!((keep >> gid[i]) & 1u)) ok &= ~(1u << i);
     }
 
     // softmax normaliser over all E logits
@@ -305,17 +315,21 @@ int topk(const float* scores, const float* bias, int T, const moe_route_cfg* c, 
     const int E = c->num_experts;
     const int blocks = moe::ceil_div(T, TOPK_THREADS / 32);
     const int sig = c->score_fn == MOE_SCORE_SIGMOID;
-#define MOE_TOPK(EPL)                                                                          \
-    topk_kernel<EPL><<<blocks, TOPK_THREADS, 0, s>>>(scores, bias, T, E, c->top_k, c->n_group, \
+#define MOE_TOPK(EPL, G32)                                                                     \
+    topk_kernel<EPL, G32><<<blocks, TOPK_THREADS, 0, s>>>(scores, bias, T, E, c->top_k, c->n_group, \
                                             c->topk_group, sig, c->routed_scale, idx, w, partial, \
                                             ksplit, scores_out)
     const int epl = moe::ceil_div(E, 32);
-    if (epl <= 1) MOE_TOPK(1);
-    else if (epl <= 2) MOE_TOPK(2);
-    else if (epl <= 4) MOE_TOPK(4);
-    else if (epl <= 8) MOE_TOPK(8);
-    else if (epl <= 16) MOE_TOPK(16);
-    else MOE_TOPK(32);
+    const bool g32 = c->n_group > 1 && E == 32 * c->n_group;
+    if (g32 && epl == 2) MOE_TOPK(2, true);
+    else if (g32 && epl == 4) MOE_TOPK(4, true);
+    else if (g32 && epl == 8) MOE_TOPK(8, true);
+    else if (epl <= 1) MOE_TOPK(1, false);
+    else if (epl <= 2) MOE_TOPK(2, false);
+    else if (epl <= 4) MOE_TOPK(4, false);
+    else if (epl <= 8) MOE_TOPK(8, false);
+    else if (epl <= 16) MOE_TOPK(16, false);
+    else MOE_TOPK(32, false);
 #undef MOE_TOPK
     return moe_host::launch_status();
 }

@@ -25,6 +25,8 @@ CASES = [
     (333, 64, 6, 1, 1, "sigmoid", True, 4, 1.0),
     (128, 1024, 32, 32, 8, "sigmoid", True, None, 2.5),   # largest E and k supported
     (65, 40, 5, 1, 1, "softmax", False, 1, 1.7),          # E not a multiple of 32
+    (500, 64, 6, 2, 1, "sigmoid", True, 3, 1.0),          # two groups of 32
+    (500, 128, 8, 4, 2, "sigmoid", True, 3, 2.5),         # four groups of 32
 ]
 
 
