@@ -34,17 +34,21 @@ UNIT = "tokens/s"
 L2_FLUSH_BYTES = 512 << 20
 
 
-def launches_per_step(cfg, two_streams: bool) -> int:
+def launches_per_step(cfg, two_streams: bool, fused: bool = False) -> int:
     """Our kernels per moe_layer call."""
-    n = 5  # top-k, count+scan, permute, combine, router GEMM
+    n = 4  # top-k, count+scan, permute, router GEMM
+    if not fused:
+        n += 1  # combine
     if cfg.dtype == "bf16":
         n += 1  # router weight split
     n += 2  # gate/up and down grouped GEMMs (routed)
     if cfg.shared_I:
-        if cfg.dtype == "bf16" and cfg.shared_I == cfg.I:
-            n += 1 if two_streams else 0  # shared gate/up on the second stream
+        if cfg.dtype == "bf16" and cfg.shared_I == cfg.I and (not two_streams or fused):
+            # its tiles ride in the routed launches (fused: its gate/up on the
+            # second stream)
+            n += 1 if two_streams else 0
         else:
-            n += 2  # separate shared-expert launches
+            n += 2  # its own two launches
     return n
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the routed
@@ -432,11 +436,13 @@ def run_ours(args, cfg):
     gu_flops = 2.0 * S * d * 2 * I
     dn_bytes = active * d * I * es + S * I * es + S * d * 4
     dn_flops = 2.0 * S * I * d
-    # bf16, I_sh == I: the shared expert's down tiles run in the routed down
-    # launch; its gate/up tiles in the routed gate/up launch only without a
-    # second stream (with one, they run in a launch of their own)
+    # bf16, I_sh == I: with a second stream the shared expert runs there in
+    # launches of its own (with the fused combine, only its gate/up; its down
+    # tiles ride in the routed down launch); without one, both halves ride
+    # in the routed launches
     two_streams = layer.stream2 is not None
-    merged = bool(cfg.shared_I) and cfg.dtype == "bf16" and cfg.shared_I == cfg.I
+    merged = (bool(cfg.shared_I) and cfg.dtype == "bf16" and cfg.shared_I == cfg.I
+              and (not two_streams or args.fused_combine))
     merged_gu = merged and not two_streams
     Is = cfg.shared_I
     if merged_gu:
@@ -516,7 +522,7 @@ def run_ours(args, cfg):
         cpu = cpu_baseline(cfg, inp)
 
     if rank == 0:
-        launches = launches_per_step(cfg, two_streams) * K
+        launches = launches_per_step(cfg, two_streams, args.fused_combine) * K
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": warm, "ms_per_step": 1e3 * total_s / K, "higher_is_better": True,

@@ -351,13 +351,16 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
         if (rc == MOE_OK && stage[i] && cudaEventRecord(stage[i], s0) != cudaSuccess) rc = MOE_ERR_CUDA;
     };
     mark(0);
-    // bf16 with a shared expert of the routed experts' size: its down tiles
-    // run inside the routed down launch; its gate/up runs on stream2 (when
-    // given) while the routing and dispatch kernels leave the tensor cores
-    // idle, else inside the routed gate/up launch.  Other shapes: the shared
-    // expert as launches of its own, on stream2 when given.
-    const bool merged = sh && a->dtype == MOE_BF16 && a->I_sh == I;
+    // Where the shared expert runs.  Given stream2, both of its GEMMs run
+    // there while the routing and dispatch kernels leave the tensor cores
+    // idle, and the combine waits for them.  With the fused combine (bf16,
+    // I_sh == I) its down tiles ride in the routed down launch instead,
+    // which adds them into the output.  Without stream2, bf16 with I_sh == I
+    // puts both of its halves into the routed launches; other shapes run it
+    // as launches of its own on the main stream.
     const bool two_streams = s1 && s1 != s0;
+    const bool fits = sh && a->dtype == MOE_BF16 && a->I_sh == I;
+    const bool merged = fits && (!two_streams || (a->flags & MOE_LAYER_FUSED_COMBINE));
     moe_tc::SharedExpert shx{a->x, T, a->w13_sh, a->w2_sh, w.hsh, w.ysh,
                              /*in_gate_up=*/!two_streams, /*in_down=*/true};
     cudaEvent_t ev_start = nullptr, ev_shared = nullptr;
@@ -373,7 +376,8 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     // leaves idle, then continue beside the top-k and dispatch kernels.
     // Measured on DeepSeek-V3 prefill: 4.129 ms vs 4.157 ms when started
     // after the router GEMM, which in turn beat starting before the router
-    // (its CTAs then delayed the router).
+    // (its CTAs then delayed the router); both GEMMs there rather than its
+    // down tiles in the routed down launch: 4.057 vs 4.110 ms.
     if (rc == MOE_OK)
         rc = run_route(a->x, a->dtype, a->w_router, a->bias, T, d, &a->route, w.scores, w.idx, w.w,
                        w.wsplit, w.err, ctr(w.err, CTR_ROUTER), s0, overlap ? ev_start : nullptr);

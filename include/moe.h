@@ -210,12 +210,13 @@ size_t moe_layer_workspace_size(const moe_layer_args* a);
 
 /* out [T,d] fp32 = the layer: route, dispatch, grouped FFN, shared expert,
  * combine.  `stream2` (may be NULL) is a second stream of the same device.
- * With bf16 and I_sh == I the shared expert's down tiles run inside the
- * routed down launch, and its gate/up runs on stream2 (launched with the
- * router GEMM, concurrently with it, top-k and dispatch) or, without stream2,
- * inside the routed gate/up launch.  Other shapes run the shared expert as
- * launches of its own, on stream2 when given.  Streams are ordered by events;
- * everything is complete on `stream` when the call's work finishes there. */
+ * Given stream2, the shared expert's two GEMMs run there, launched with the
+ * router GEMM and concurrent with it, top-k and dispatch (with
+ * MOE_LAYER_FUSED_COMBINE only its gate/up; its down tiles then ride in the
+ * routed down launch).  Without stream2, bf16 with I_sh == I runs the shared
+ * expert's tiles inside the routed launches; other shapes run it as launches
+ * of its own on `stream`.  Streams are ordered by events; everything is
+ * complete on `stream` when the call's work finishes there. */
 int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, void* stream,
               void* stream2);
 
