@@ -183,8 +183,9 @@ int check_layer_sizes(const moe_layer_args* a) {
 int check_layer(const moe_layer_args* a) {
     int rc = check_layer_sizes(a);
     if (rc != MOE_OK) return rc;
-    if (!a->x || !a->w_router || !a->w13 || !a->w2) return MOE_ERR_INVALID_ARG;
-    if (!moe_host::aligned16(a->x) || !moe_host::aligned16(a->w_router) ||
+    // x may be NULL for an empty batch (T == 0)
+    if ((a->T > 0 && !a->x) || !a->w_router || !a->w13 || !a->w2) return MOE_ERR_INVALID_ARG;
+    if ((a->x && !moe_host::aligned16(a->x)) || !moe_host::aligned16(a->w_router) ||
         !moe_host::aligned16(a->w13) || !moe_host::aligned16(a->w2))
         return MOE_ERR_INVALID_ARG;
     if (a->bias && a->route.score_fn == MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
@@ -334,7 +335,7 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
               void* stream2) {
     int rc = check_layer(a);
     if (rc != MOE_OK) return rc;
-    if (!out || !moe_host::aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if ((a->T > 0 && !out) || (out && !moe_host::aligned16(out))) return MOE_ERR_INVALID_ARG;
     if (!ws || !moe_host::aligned16(ws) || ws_bytes < carve_layer(a, nullptr).total)
         return MOE_ERR_WORKSPACE;
     const LayerWs w = carve_layer(a, ws);
@@ -342,7 +343,13 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     cudaStream_t s0 = static_cast<cudaStream_t>(stream);
     cudaStream_t s1 = static_cast<cudaStream_t>(stream2);
     if (cudaMemsetAsync(w.err, 0, HDR_CLEAR, s0) != cudaSuccess) return MOE_ERR_CUDA;
-    if (T == 0) return MOE_OK;
+    if (T == 0) {
+        // an empty batch: every expert gets zero rows
+        if (a->offsets_out &&
+            cudaMemsetAsync(a->offsets_out, 0, sizeof(int32_t) * (size_t)(E + 1), s0) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
     const bool sh = w.ysh != nullptr;
     cudaEvent_t stage[MOE_LAYER_EVENTS] = {};
     if (a->stage_events)

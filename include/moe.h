@@ -216,7 +216,9 @@ size_t moe_layer_workspace_size(const moe_layer_args* a);
  * routed down launch).  Without stream2, bf16 with I_sh == I runs the shared
  * expert's tiles inside the routed launches; other shapes run it as launches
  * of its own on `stream`.  Streams are ordered by events; everything is
- * complete on `stream` when the call's work finishes there. */
+ * complete on `stream` when the call's work finishes there.  T = 0 is an
+ * empty batch: x and out may be NULL, only offsets_out (if given) is written
+ * (zeros). */
 int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, void* stream,
               void* stream2);
 

@@ -258,3 +258,19 @@ def test_layer_cuda_graph_replay(oracle, cfg):
         layer.forward(xn, topk_idx_out=idx)
         same = (np_(idx) == ridx).all(1)
         assert_bf16_close(np_(out)[same], rout[same], cfg.name)
+
+
+def test_layer_empty_batch():
+    """T = 0: nothing to compute; the call succeeds and reports every expert
+    empty."""
+    cfg = SMALL_BF16[0].with_(T=0)
+    inp = inputs.make_inputs(cfg, seed=1, device="cuda")
+    layer = B.MoELayer(inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"],
+                       inp["w2_sh"], B.cfg_from(cfg), 0)
+    offs = torch.full((cfg.E + 1,), -1, dtype=torch.int32, device="cuda")
+    out = layer.forward(inp["x"], offsets_out=offs)
+    torch.cuda.synchronize()
+    assert out.shape == (0, cfg.d)
+    assert (offs == 0).all()
+    rc, detail = B.moe_check_error(layer.ws)
+    assert rc == B.OK, detail
