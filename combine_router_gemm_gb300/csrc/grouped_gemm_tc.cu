@@ -315,11 +315,13 @@ struct Unit {
 // Inside a stream, units are expert-major (units of expert e occupy
 // [pre[e]*nt, pre[e+1]*nt)), then feature tile, then token tile, so CTAs that
 // run together share an expert's token tiles and weight tiles in L2.
-// Measured (Zipf workload, 16384 tokens): 11.94 ms with a 256-row class
-// threshold, 12.14 ms with 512, 12.31 ms with one stream; other workloads
-// unchanged.
+// Measured: with a 128-row class threshold DeepSeek-V3 prefill (4096
+// tokens) takes 4.106 ms per layer against 4.137 ms with 256 (the down
+// GEMM 1.302 vs 1.325 ms), the Zipf workload (16384 tokens) 10.69 vs
+// 10.71-10.75 ms; 512 and 1024 rows are slower on Zipf (10.85, 10.94 ms),
+// and one stream was slower still when first measured.
 #ifndef MOE_COMPUTE_ROWS
-#define MOE_COMPUTE_ROWS 256
+#define MOE_COMPUTE_ROWS 128
 #endif
 
 struct Sched {
