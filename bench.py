@@ -57,12 +57,12 @@ def launches_per_step(cfg, two_streams: bool, fused: bool = False) -> int:
 # scaled x8 (experts and tokens) and the shared expert's weights are not
 # (profiles/grouped_gemm_tc_dsv3_prefill_e32.md).  Reported as null once the
 # kernel source no longer matches the captured one.
-TRAFFIC = {"source_sha256": "95e685d0a248fa5dc73834f1498701a5ae9d1e6df9bd26a437a190defa539b54",
-           # routed gate/up launch (the shared expert's gate/up runs on the
-           # second stream): dsv3_prefill from a one-pass capture of the full
-           # layer, dsv3_prefill_e32 from a capture of the 32-expert case
-           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.960355e9,
-                                            "dsv3_prefill": 15.886749e9}}
+TRAFFIC = {"source_sha256": "43f0c4a3734291ddb3595305f1c70d1b295cdbc48832ba922349073bbe4badb9",
+           # routed gate/up launch (the shared expert runs on the second
+           # stream): dsv3_prefill from a one-pass capture of the full layer,
+           # dsv3_prefill_e32 from a capture of the 32-expert case
+           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.968e9,
+                                            "dsv3_prefill": 15.820377e9}}
 
 
 def peaks():
