@@ -61,7 +61,7 @@ TRAFFIC = {"source_sha256": "43f0c4a3734291ddb3595305f1c70d1b295cdbc48832ba92234
            # routed gate/up launch (the shared expert runs on the second
            # stream): dsv3_prefill from a one-pass capture of the full layer,
            # dsv3_prefill_e32 from a capture of the 32-expert case
-           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.968e9,
+           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.969214e9,
                                             "dsv3_prefill": 15.820377e9}}
 
 
