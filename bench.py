@@ -363,7 +363,7 @@ def run_ours(args, cfg):
     inp = inputs.make_inputs(cfg, seed=0, device="cuda")
     layer = B.MoELayer(inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"],
                        inp["w2_sh"], B.cfg_from(cfg), cfg.T, overlap=not args.no_overlap,
-                       fused_combine=args.fused_combine)
+                       fused_combine=args.fused_combine, pack_weights=not args.row_major_weights)
     x = inp["x"]
     out = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device="cuda")
     offs = torch.empty(cfg.E + 1, dtype=torch.int32, device="cuda")
@@ -527,7 +527,9 @@ def run_ours(args, cfg):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": warm, "ms_per_step": 1e3 * total_s / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
-            "config": config_dict(cfg), "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "config": {**config_dict(cfg), "expert_weights": "tile-major, packed once at layer "
+                       "construction" if layer.packed else "row-major"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clk.summary(), "stages": stages,
             "active_experts": active, "wall_s_timed": round(t_wall, 3),
         }
@@ -555,6 +557,8 @@ def main():
     ap.add_argument("--no-comparators", action="store_true",
                     help="skip the PyTorch comparator (the eager layer)")
     ap.add_argument("--no-overlap", action="store_true", help="shared expert on the main stream")
+    ap.add_argument("--row-major-weights", action="store_true",
+                    help="keep the expert weights row-major (no tile-major packing)")
     ap.add_argument("--fused-combine", action="store_true",
                     help="add the down projection's results straight into the output (atomics)")
     args = ap.parse_args()

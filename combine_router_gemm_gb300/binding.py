@@ -26,7 +26,8 @@ SYMBOLS = ("moe_status_string", "moe_version", "moe_route_from_scores", "moe_rou
            "moe_route_workspace_size",
            "moe_dispatch_workspace_size", "moe_dispatch", "moe_grouped_ffn_workspace_size",
            "moe_grouped_ffn", "moe_combine", "moe_layer_workspace_size", "moe_layer",
-           "moe_check_error", "moe_dispatch_noalloc", "moe_selftest_bounded_wait")
+           "moe_check_error", "moe_dispatch_noalloc", "moe_selftest_bounded_wait",
+           "moe_pack_expert_weights")
 
 
 class MoEError(RuntimeError):
@@ -52,6 +53,7 @@ class LayerArgs(ctypes.Structure):
                 ("flags", ctypes.c_int32)]
 
 LAYER_FUSED_COMBINE = 1
+LAYER_PACKED_WEIGHTS = 2
 
 LAYER_EVENTS = 7
 
@@ -99,6 +101,8 @@ def load() -> ctypes.CDLL:
     lib.moe_dispatch_noalloc.restype = i32
     lib.moe_selftest_bounded_wait.argtypes = [i32, ctypes.c_uint32, P, sz, P]
     lib.moe_selftest_bounded_wait.restype = i32
+    lib.moe_pack_expert_weights.argtypes = [P, P, i32, i32, i32, P, P, P]
+    lib.moe_pack_expert_weights.restype = i32
     _lib = lib
     return lib
 
@@ -316,23 +320,67 @@ def moe_check_error(ws, stream=None) -> tuple[int, int]:
 
 # ---------------------------------------------------------------- convenience
 
+def moe_pack_expert_weights(w13, w2, w13_packed, w2_packed, stream=None):
+    """w13 [E,2I,d] and w2 [E,d,I] bf16 (either may be None, with its output)
+    into the tile-major layouts of LAYER_PACKED_WEIGHTS; 2-D shared-expert
+    weights ([2I,d], [d,I]) are packed as E = 1."""
+    ref = w13 if w13 is not None else w2
+    if ref is None:
+        return
+    if ref.dim() == 2:
+        E = 1
+        d = w13.shape[1] if w13 is not None else w2.shape[0]
+        I = w13.shape[0] // 2 if w13 is not None else w2.shape[1]
+    else:
+        E = ref.shape[0]
+        d = w13.shape[2] if w13 is not None else w2.shape[1]
+        I = w13.shape[1] // 2 if w13 is not None else w2.shape[2]
+    rc = load().moe_pack_expert_weights(_ptr(w13, torch.bfloat16, "w13"),
+                                        _ptr(w2, torch.bfloat16, "w2"), E, d, I,
+                                        _ptr(w13_packed, torch.bfloat16, "w13_packed"),
+                                        _ptr(w2_packed, torch.bfloat16, "w2_packed"),
+                                        _stream(stream))
+    _check(rc, "moe_pack_expert_weights")
+
+
+def packable(w13, w2, w13_sh=None, w2_sh=None) -> bool:
+    """Whether the tile-major layouts apply (bf16, I % 128 == 0, d % 256 == 0)."""
+    if w13.dtype != torch.bfloat16:
+        return False
+    d, I = w13.shape[2], w2.shape[2]
+    I_sh = w2_sh.shape[1] if w2_sh is not None else 0
+    return d % 256 == 0 and I % 128 == 0 and I_sh % 128 == 0
+
+
 class MoELayer:
     """Holds the weights of one layer plus a workspace; ``forward(x)`` -> out fp32 [T,d].
 
     ``x`` must have the token count the layer was built for (workspace size
     depends on it).  Allocation happens only here, in PyTorch, never in the
-    library.
+    library.  With ``pack_weights`` (the default) the expert weights are
+    copied once into the tile-major layouts the grouped GEMMs stream fastest,
+    where the shapes allow it; the layer then holds those copies.
     """
 
     def __init__(self, w_router, bias, w13, w2, w13_sh, w2_sh, cfg: RouteCfg, T: int,
-                 overlap: bool = True, fused_combine: bool = False):
-        self.w = dict(w_router=w_router, bias=bias, w13=w13, w2=w2, w13_sh=w13_sh, w2_sh=w2_sh)
+                 overlap: bool = True, fused_combine: bool = False, pack_weights: bool = True):
         self.cfg = cfg
         self.T = T
         dev = w13.device
         d = w13.shape[2]
         I_sh = w2_sh.shape[1] if w2_sh is not None else 0
         self.flags = LAYER_FUSED_COMBINE if fused_combine else 0
+        self.packed = pack_weights and packable(w13, w2, w13_sh, w2_sh)
+        if self.packed:
+            p13, p2 = torch.empty_like(w13), torch.empty_like(w2)
+            moe_pack_expert_weights(w13, w2, p13, p2)
+            w13, w2 = p13, p2
+            if w13_sh is not None:
+                p13s, p2s = torch.empty_like(w13_sh), torch.empty_like(w2_sh)
+                moe_pack_expert_weights(w13_sh, w2_sh, p13s, p2s)
+                w13_sh, w2_sh = p13s, p2s
+            self.flags |= LAYER_PACKED_WEIGHTS
+        self.w = dict(w_router=w_router, bias=bias, w13=w13, w2=w2, w13_sh=w13_sh, w2_sh=w2_sh)
         sizes = LayerArgs(None, None, None, None, None, None, None, T, d, w2.shape[2], I_sh,
                           _dtype_code(w13), cfg, None, None, None, None, None, self.flags)
         self.ws_bytes = moe_layer_workspace_size(sizes)

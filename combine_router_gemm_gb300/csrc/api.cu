@@ -72,14 +72,14 @@ size_t ffn_ws(int rows, int d, int I, int dtype) {
 
 int run_ffn(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
             const void* w13, const void* w2, int dtype, float* y, void* h, uint32_t* err,
-            unsigned* work, cudaStream_t s, cudaEvent_t between = nullptr) {
+            unsigned* work, cudaStream_t s, cudaEvent_t between = nullptr, bool packed = false) {
     if (rows == 0) {
         if (between && cudaEventRecord(between, s) != cudaSuccess) return MOE_ERR_CUDA;
         return MOE_OK;
     }
     if (dtype == MOE_BF16)
         return moe_tc::grouped_ffn_bf16(x_perm, offsets, E, rows, d, I, w13, w2, y, h, err, work,
-                                        s, between);
+                                        s, between, nullptr, nullptr, 3, nullptr, packed);
     int rc = moe_f32::grouped_ffn_f32(static_cast<const float*>(x_perm), offsets, E, rows, d, I,
                                       static_cast<const float*>(w13), static_cast<const float*>(w2),
                                       y, static_cast<float*>(h), err, s);
@@ -198,7 +198,10 @@ int check_layer(const moe_layer_args* a) {
     const void* outs[] = {a->scores_out, a->topk_idx_out, a->topk_w_out, a->offsets_out};
     for (const void* o : outs)
         if (o && !moe_host::aligned16(o)) return MOE_ERR_INVALID_ARG;
-    if (a->flags & ~MOE_LAYER_FUSED_COMBINE) return MOE_ERR_INVALID_ARG;
+    if (a->flags & ~(MOE_LAYER_FUSED_COMBINE | MOE_LAYER_PACKED_WEIGHTS)) return MOE_ERR_INVALID_ARG;
+    if ((a->flags & MOE_LAYER_PACKED_WEIGHTS) &&
+        (a->dtype != MOE_BF16 || a->I % 128 != 0 || a->d % 256 != 0 || a->I_sh % 128 != 0))
+        return MOE_ERR_UNSUPPORTED;
     if ((a->flags & MOE_LAYER_FUSED_COMBINE) &&
         (a->dtype != MOE_BF16 || (a->I_sh > 0 && a->I_sh != a->I)))
         return MOE_ERR_UNSUPPORTED;
@@ -395,6 +398,7 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     // on stream2 (before the shared expert, which the down launch waits for)
     // when given, so that the main stream does not pay for it
     const bool zero_on_s1 = fused && merged && overlap;
+    const bool packed = a->flags & MOE_LAYER_PACKED_WEIGHTS;
     if (overlap) {
         if (rc == MOE_OK && cudaStreamWaitEvent(s1, ev_start, 0) != cudaSuccess) rc = MOE_ERR_CUDA;
         if (rc == MOE_OK && zero_on_s1 &&
@@ -404,10 +408,10 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
             if (merged)  // gate/up only; the down tiles ride in the routed launch
                 rc = moe_tc::grouped_ffn_bf16(a->x, nullptr, 1, T, d, I, a->w13_sh, a->w2_sh, w.ysh,
                                               w.hsh, w.err, ctr(w.err, CTR_SHARED), s1, nullptr,
-                                              nullptr, nullptr, /*parts=*/1);
+                                              nullptr, nullptr, /*parts=*/1, nullptr, packed);
             else
                 rc = run_ffn(a->x, nullptr, 1, T, d, a->I_sh, a->w13_sh, a->w2_sh, a->dtype, w.ysh,
-                             w.hsh, w.err, ctr(w.err, CTR_SHARED), s1);
+                             w.hsh, w.err, ctr(w.err, CTR_SHARED), s1, nullptr, packed);
         }
         if (rc == MOE_OK && cudaEventRecord(ev_shared, s1) != cudaSuccess) rc = MOE_ERR_CUDA;
     }
@@ -424,15 +428,15 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
             rc = moe_tc::grouped_ffn_bf16(w.xp, w.offsets, E, T * k, d, I, a->w13, a->w2, w.yp, w.h,
                                           w.err, ctr(w.err, CTR_FFN), s0, stage[4],
                                           merged ? &shx : nullptr, fused ? &fc : nullptr, 3,
-                                          merged && overlap ? ev_shared : nullptr);
+                                          merged && overlap ? ev_shared : nullptr, packed);
         else
             rc = run_ffn(w.xp, w.offsets, E, T * k, d, I, a->w13, a->w2, a->dtype, w.yp, w.h,
-                         w.err, ctr(w.err, CTR_FFN), s0, stage[4]);
+                         w.err, ctr(w.err, CTR_FFN), s0, stage[4], packed);
     }
     mark(5);
     if (rc == MOE_OK && sh && !merged && !overlap)
         rc = run_ffn(a->x, nullptr, 1, T, d, a->I_sh, a->w13_sh, a->w2_sh, a->dtype, w.ysh, w.hsh,
-                     w.err, ctr(w.err, CTR_SHARED), s0);
+                     w.err, ctr(w.err, CTR_SHARED), s0, nullptr, packed);
     if (rc == MOE_OK && overlap && !merged && cudaStreamWaitEvent(s0, ev_shared, 0) != cudaSuccess)
         rc = MOE_ERR_CUDA;
     if (rc == MOE_OK && !fused)
@@ -440,6 +444,21 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     mark(6);
     if (ev_start) cudaEventDestroy(ev_start);
     if (ev_shared) cudaEventDestroy(ev_shared);
+    return rc;
+}
+
+int moe_pack_expert_weights(const void* w13, const void* w2, int E, int d, int I,
+                            void* w13_packed, void* w2_packed, void* stream) {
+    if (E < 1 || d < 256 || d % 256 != 0 || I < 128 || I % 128 != 0) return MOE_ERR_INVALID_ARG;
+    if (!w13 != !w13_packed || !w2 != !w2_packed) return MOE_ERR_INVALID_ARG;
+    for (const void* p : {w13, w2, static_cast<const void*>(w13_packed),
+                          static_cast<const void*>(w2_packed)})
+        if (p && !moe_host::aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if ((long long)E * 2 * I * d > (1ll << 40)) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = MOE_OK;
+    if (w13) rc = moe_tc::pack_weights(w13, E, 2 * I, d, /*pairs=*/false, w13_packed, s);
+    if (rc == MOE_OK && w2) rc = moe_tc::pack_weights(w2, E, d, I, /*pairs=*/true, w2_packed, s);
     return rc;
 }
 

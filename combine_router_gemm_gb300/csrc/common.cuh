@@ -87,7 +87,10 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
                      const void* w13, const void* w2, float* y, void* h, uint32_t* err,
                      unsigned* work, cudaStream_t s, cudaEvent_t between = nullptr,
                      const SharedExpert* sh = nullptr, const FusedCombine* fc = nullptr,
-                     int parts = 3, cudaEvent_t before_down = nullptr);
+                     int parts = 3, cudaEvent_t before_down = nullptr, bool packed = false);
+// Expert weights [E, rows, K] bf16 into the tile-major layout (pairs: the
+// down projection's), on stream s.  rows % 128 == 0 (pairs: % 256), K % 64 == 0.
+int pack_weights(const void* w, int E, int rows, int K, bool pairs, void* out, cudaStream_t s);
 size_t router_ws_bytes(int T, int E, int d);
 int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s);
 // after_split: recorded once the weight split is done, before the GEMM

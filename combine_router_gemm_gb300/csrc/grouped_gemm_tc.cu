@@ -127,6 +127,21 @@ struct Cfg {
     static_assert(SMEM + 64 <= (size_t)SMEM_LIMIT, "shared memory over the per-CTA limit");
 };
 
+// Weight layouts.  Row-major: [rows, K] as given.  Tile-major (written by
+// moe_pack_expert_weights, rows a multiple of 128, K of 64): tile (r, kb) --
+// rows 128r..128r+127, columns 64kb..64kb+63 -- is one contiguous 16 KB
+// block, so each TMA load of a weight tile reads 16 KB in a row of HBM
+// instead of 128 pieces of 128 B one matrix row apart.  WEIGHTS_TILES orders
+// the tiles (r, kb) row-tile-major; WEIGHTS_TILE_PAIRS keeps row tiles 2m and
+// 2m+1 of each k-block next to each other, the two feature tiles that one
+// down-projection unit loads per stage.
+constexpr int WEIGHTS_ROWS = 0, WEIGHTS_TILES = 1, WEIGHTS_TILE_PAIRS = 2;
+
+__host__ __device__ __forceinline__ int packed_tile(int rt, int kb, int num_kb, int layout) {
+    return layout == WEIGHTS_TILE_PAIRS ? ((rt >> 1) * num_kb + kb) * 2 + (rt & 1)
+                                        : rt * num_kb + kb;
+}
+
 // Tensor maps of one activation matrix with token boxes of 32, 64, 128 and
 // 256 rows (index = log2(rows / 32)).
 struct BMaps {
@@ -159,6 +174,9 @@ struct Params {
     float* comb_out;
     const int32_t* row_token;
     const float* w_row;
+    // layout of the weight (A) matrix: WEIGHTS_ROWS (row-major), or one of
+    // the tile-major layouts written by moe_pack_expert_weights
+    int a_layout;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -559,9 +577,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t fb = smem_u32(&full_bar[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
                     const int kx = kb * BK;
+                    if (MODE != 2 && p.a_layout != WEIGHTS_ROWS) {
+                        // tile-major weights: one 128 x 64 tile is 16 KB in a row,
+                        // seen through the map as 128 rows of 64 elements
 #pragma unroll
-                    for (int a = 0; a < NUM_A; ++a)
-                        tma_load_2d(smem_u32(st + a * A_TILE_BYTES), ma, fb, kx, a_row + a * p.a_step);
+                        for (int a = 0; a < NUM_A; ++a) {
+                            const int rt = (a_row + a * p.a_step) / BM;  // 128-row tile
+                            tma_load_2d(smem_u32(st + a * A_TILE_BYTES), ma, fb, 0,
+                                        packed_tile(rt, kb, num_kb, p.a_layout) * BM);
+                        }
+                    } else {
+#pragma unroll
+                        for (int a = 0; a < NUM_A; ++a)
+                            tma_load_2d(smem_u32(st + a * A_TILE_BYTES), ma, fb, kx,
+                                        a_row + a * p.a_step);
+                    }
                     // the token rows in at most four boxes of 256/128/64/32 rows
                     uint8_t* bdst = st + NUM_A * A_TILE_BYTES;
                     int row = 0;
@@ -834,6 +864,32 @@ __global__ void split_weight_kernel(const float* __restrict__ w, long n,
     }
 }
 
+// Expert weights [E, rows, K] into the tile-major layouts (see WEIGHTS_*):
+// one thread per 16-byte vector of the output, read from its source row.
+__global__ void pack_weights_kernel(const uint4* __restrict__ w, long n_vec, int rows, int K,
+                                    int pairs, uint4* __restrict__ out) {
+    const int kv = K / 8, KB = K / BK;
+    const long tiles_per_expert = (long)(rows / BM) * KB;
+    for (long v = blockIdx.x * (long)blockDim.x + threadIdx.x; v < n_vec;
+         v += (long)gridDim.x * blockDim.x) {
+        const long tile = v / (BM * BK / 8);
+        const int in = (int)(v % (BM * BK / 8));  // 128 rows of 8 vectors
+        const long e = tile / tiles_per_expert;
+        const int t = (int)(tile % tiles_per_expert);
+        int rt, kb;
+        if (pairs) {
+            const int pr = t / (2 * KB), rem = t % (2 * KB);
+            kb = rem >> 1;
+            rt = 2 * pr + (rem & 1);
+        } else {
+            rt = t / KB;
+            kb = t % KB;
+        }
+        const long src_row = e * rows + (long)rt * BM + in / 8;
+        out[v] = w[src_row * kv + (long)kb * 8 + in % 8];
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -911,36 +967,50 @@ int launch(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, const BM
 
 namespace moe_tc {
 
+// A weight matrix of `rows` rows and K columns (bf16) in the given layout.
+bool make_weight_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, bool packed) {
+    if (!packed) return make_map(m, base, rows, K, BM);
+    // tile-major: every 64 columns of every row become one 128-byte row
+    return make_map(m, base, rows * ((K + BK - 1) / BK), BK, BM);
+}
+
 // Both GEMMs of the SwiGLU FFN over bf16 rows; offsets == NULL means one
 // segment [0, rows) with expert 0 (dense).  When sh is given, the shared
 // expert (dense over sh->x, I_sh == I) runs inside the same launches (those
 // its in_gate_up / in_down flags name).  When fc is given, the down launch
-// adds its results into fc->out instead of writing y.
+// adds its results into fc->out instead of writing y.  packed: the weights
+// (and the shared expert's) are in the tile-major layouts of
+// moe_pack_expert_weights.
 int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
                      const void* w13, const void* w2, float* y, void* h, uint32_t* err,
                      unsigned* work, cudaStream_t s, cudaEvent_t between,
                      const SharedExpert* sh, const FusedCombine* fc, int parts,
-                     cudaEvent_t before_down) {
+                     cudaEvent_t before_down, bool packed) {
     if (E > MAX_E) return MOE_ERR_UNSUPPORTED;
     CUtensorMap a1, a2, a1s, a2s;
     BMaps b1, b2, b1s, b2s;
-    if (!make_map(&a1, w13, (uint64_t)E * 2 * I, d, BM) || !make_bmaps(&b1, x_perm, rows, d) ||
-        !make_map(&a2, w2, (uint64_t)E * d, I, BM) || !make_bmaps(&b2, h, rows, I))
+    if (!make_weight_map(&a1, w13, (uint64_t)E * 2 * I, d, packed) ||
+        !make_bmaps(&b1, x_perm, rows, d) ||
+        !make_weight_map(&a2, w2, (uint64_t)E * d, I, packed) || !make_bmaps(&b2, h, rows, I))
         return MOE_ERR_CUDA;
     const bool two = sh != nullptr && sh->T > 0;
     if (two) {
-        if (!make_map(&a1s, sh->w13, 2ull * I, d, BM) || !make_bmaps(&b1s, sh->x, sh->T, d) ||
-            !make_map(&a2s, sh->w2, (uint64_t)d, I, BM) || !make_bmaps(&b2s, sh->h, sh->T, I))
+        if (!make_weight_map(&a1s, sh->w13, 2ull * I, d, packed) ||
+            !make_bmaps(&b1s, sh->x, sh->T, d) ||
+            !make_weight_map(&a2s, sh->w2, (uint64_t)d, I, packed) ||
+            !make_bmaps(&b2s, sh->h, sh->T, I))
             return MOE_ERR_CUDA;
     } else {
         a1s = a1; b1s = b1; a2s = a2; b2s = b2;
     }
     const bool two_gu = two && sh->in_gate_up, two_dn = two && sh->in_down;
     Params p1{offsets, E,   rows, d, I, 2 * I, I, h, err, 0, two_gu ? sh->T : 0,
-              two_gu ? sh->h : nullptr, work};
+              two_gu ? sh->h : nullptr, work, 1, nullptr, nullptr, nullptr,
+              packed ? WEIGHTS_TILES : WEIGHTS_ROWS};
     Params p2{offsets, E, rows, I, d, d, BM, y, err, 0, two_dn ? sh->T : 0,
               two_dn ? sh->y : nullptr, work + 1, 1, fc ? fc->out : nullptr,
-              fc ? fc->row_token : nullptr, fc ? fc->w_row : nullptr};
+              fc ? fc->row_token : nullptr, fc ? fc->w_row : nullptr,
+              packed ? WEIGHTS_TILE_PAIRS : WEIGHTS_ROWS};
     // Token tile per launch, from the average rows per expert (the host does
     // not see the device-side offsets).  A weight-streaming GEMM runs at the
     // rate (k-blocks in flight per SM) / (load latency), so the tile trades
@@ -973,6 +1043,15 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     if (before_down && cudaStreamWaitEvent(s, before_down, 0) != cudaSuccess) return MOE_ERR_CUDA;
     return dn_wide ? launch<1, MOE_DN_BN>(a2, b2, a2s, b2s, p2, s, dn_units)
                    : launch<1, 128>(a2, b2, a2s, b2s, p2, s, dn_units);
+}
+
+int pack_weights(const void* w, int E, int rows, int K, bool pairs, void* out, cudaStream_t s) {
+    const long n_vec = (long)E * rows * (K / 8);
+    if (n_vec == 0) return MOE_OK;
+    const int blocks = (int)std::min<long>((n_vec + 255) / 256, 8L * moe_host::num_sms());
+    pack_weights_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(w), n_vec, rows, K,
+                                               pairs ? 1 : 0, static_cast<uint4*>(out));
+    return moe_host::launch_status();
 }
 
 int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s) {

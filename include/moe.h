@@ -202,6 +202,13 @@ typedef struct {
  * order then varies from run to run (results agree to fp32 rounding). */
 #define MOE_LAYER_FUSED_COMBINE 1
 
+/* moe_layer_args.flags: w13 and w2 (and w13_sh, w2_sh) are in the tile-major
+ * layouts written by moe_pack_expert_weights, which the grouped GEMMs stream
+ * faster.  bf16 with I % 128 == 0, d % 256 == 0 and I_sh % 128 == 0 only
+ * (else MOE_ERR_UNSUPPORTED).  Results are the same, bit for bit, as with
+ * the row-major weights they were packed from. */
+#define MOE_LAYER_PACKED_WEIGHTS 2
+
 /* Workspace bytes moe_layer needs (0 for invalid sizes or configuration).
  * Only the sizes, dtype, routing configuration, I_sh (> 0: shared expert
  * present) and which optional outputs are non-NULL matter here; the input
@@ -221,6 +228,22 @@ size_t moe_layer_workspace_size(const moe_layer_args* a);
  * (zeros). */
 int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, void* stream,
               void* stream2);
+
+/* Expert weights into the tile-major layouts of MOE_LAYER_PACKED_WEIGHTS, a
+ * one-time preparation of a layer's weights.  Each 128-row x 64-column tile
+ * (16 KB of bf16) is stored contiguously, so that the grouped GEMMs read it
+ * from HBM in one piece rather than as 128 pieces one matrix row apart.
+ *   w13 [E, 2I, d] -> w13_packed, tiles (row tile r, column block c) in the
+ *     order r-major then c; w2 [E, d, I] -> w2_packed, the two row tiles
+ *     2m, 2m+1 of each column block next to each other (the two feature tiles
+ *     one down-projection unit reads per stage).  Same sizes as the inputs.
+ *   The shared expert's w13_sh [2I_s, d] and w2_sh [d, I_s]: call with E = 1.
+ *   Either pair (w13, w13_packed) or (w2, w2_packed) may be NULL (skipped).
+ *   Requirements: I % 128 == 0, d % 256 == 0, E >= 1, 16-byte aligned device
+ *   pointers (MOE_ERR_INVALID_ARG otherwise); outputs must not overlap the
+ *   inputs.  Asynchronous on `stream`. */
+int moe_pack_expert_weights(const void* w13, const void* w2, int E, int d, int I,
+                            void* w13_packed, void* w2_packed, void* stream);
 
 /* ------------------------------------------------- allocation-free dispatch */
 

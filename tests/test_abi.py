@@ -143,3 +143,29 @@ def test_layer_rejects(lib):
                                                           w_router=None))) == need
     # the optional outputs replace workspace regions
     assert lib.moe_layer_workspace_size(ctypes.byref(args(scores_out=P))) < need
+
+
+def test_pack_expert_weights_rejects(lib):
+    # the valid form launches a kernel (tests/test_gpu_ffn.py)
+    assert lib.moe_pack_expert_weights(*[P, P, 4, 200, 128, P, P, None]) == B.ERR_INVALID_ARG  # d % 256
+    assert lib.moe_pack_expert_weights(*[P, P, 4, 256, 136, P, P, None]) == B.ERR_INVALID_ARG  # I % 128
+    assert lib.moe_pack_expert_weights(*[P, P, 0, 256, 128, P, P, None]) == B.ERR_INVALID_ARG  # E
+    assert lib.moe_pack_expert_weights(*[P, P, 4, 256, 128, None, P, None]) == B.ERR_INVALID_ARG  # pairing
+    assert lib.moe_pack_expert_weights(*[P + 8, P, 4, 256, 128, P, P, None]) == B.ERR_INVALID_ARG  # alignment
+    assert lib.moe_pack_expert_weights(None, None, 4, 256, 128, None, None, None) == B.OK  # nothing to do
+
+
+def test_layer_packed_flag_checks(lib):
+    def args(**kw):
+        a = dict(x=P, w_router=P, bias=None, w13=P, w2=P, w13_sh=None, w2_sh=None, T=64, d=256,
+                 I=256, I_sh=0, dtype=B.BF16, route=cfg(), scores_out=None, topk_idx_out=None,
+                 topk_w_out=None, offsets_out=None, flags=B.LAYER_PACKED_WEIGHTS)
+        a.update(kw)
+        return B.LayerArgs(**a)
+    need = lib.moe_layer_workspace_size(ctypes.byref(args()))
+    assert need > 0
+    for bad in (dict(d=384), dict(I=136), dict(dtype=B.F32), dict(w13_sh=P, w2_sh=P, I_sh=136)):
+        a = args(**bad)
+        n = lib.moe_layer_workspace_size(ctypes.byref(a)) or need
+        assert lib.moe_layer(ctypes.byref(a), P, P, n, None, None) == B.ERR_UNSUPPORTED, bad
+    assert lib.moe_layer(ctypes.byref(args(flags=8)), P, P, need, None, None) == B.ERR_INVALID_ARG

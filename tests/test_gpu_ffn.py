@@ -107,3 +107,34 @@ def test_grouped_ffn_bad_offsets_flagged():
     B.moe_grouped_ffn(x, offsets, w13, w2, y, ws)
     rc, detail = B.moe_check_error(ws)
     assert rc == B.ERR_DEVICE_INPUT and detail != 0
+
+
+def torch_pack(w, pairs):
+    """The tile-major layouts written out with torch view/permute."""
+    if w.dim() == 2:
+        return torch_pack(w[None], pairs)[0]
+    E, R, K = w.shape
+    if pairs:
+        t = w.view(E, R // 256, 2, 128, K // 64, 64).permute(0, 1, 4, 2, 3, 5)
+    else:
+        t = w.view(E, R // 128, 128, K // 64, 64).permute(0, 1, 3, 2, 4)
+    return t.contiguous().view(E, R, K)
+
+
+@pytest.mark.parametrize("E,d,I", [(3, 256, 128), (1, 512, 384), (2, 768, 256)])
+def test_pack_expert_weights_layout(E, d, I):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(E + d)
+    w13 = torch.randn((E, 2 * I, d), generator=g, device="cuda").to(torch.bfloat16)
+    w2 = torch.randn((E, d, I), generator=g, device="cuda").to(torch.bfloat16)
+    p13, p2 = torch.empty_like(w13), torch.empty_like(w2)
+    B.moe_pack_expert_weights(w13, w2, p13, p2)
+    torch.cuda.synchronize()
+    assert torch.equal(p13, torch_pack(w13, False))
+    assert torch.equal(p2, torch_pack(w2, True))
+    # 2-D shared-expert weights
+    s13, s2 = torch.empty_like(w13[0]), torch.empty_like(w2[0])
+    B.moe_pack_expert_weights(w13[0], w2[0], s13, s2)
+    torch.cuda.synchronize()
+    assert torch.equal(s13, torch_pack(w13[0], False))
+    assert torch.equal(s2, torch_pack(w2[0], True))

@@ -274,3 +274,23 @@ def test_layer_empty_batch():
     assert (offs == 0).all()
     rc, detail = B.moe_check_error(layer.ws)
     assert rc == B.OK, detail
+
+
+@pytest.mark.parametrize("overlap", [True, False])
+def test_layer_packed_weights_bit_identical(overlap):
+    """The layer on tile-major packed weights gives the same output, bit for
+    bit, as on the row-major weights they came from."""
+    cfg = SMALL_BF16[0]
+    inp = inputs.make_inputs(cfg, seed=8, device="cuda")
+    args = (inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"], inp["w2_sh"],
+            B.cfg_from(cfg), cfg.T)
+    packed = B.MoELayer(*args, overlap=overlap, pack_weights=True)
+    plain = B.MoELayer(*args, overlap=overlap, pack_weights=False)
+    assert packed.packed and not plain.packed
+    a = packed.forward(inp["x"])
+    b = plain.forward(inp["x"])
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    for layer in (packed, plain):
+        rc, detail = B.moe_check_error(layer.ws)
+        assert rc == B.OK, detail
