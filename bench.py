@@ -57,12 +57,13 @@ def launches_per_step(cfg, two_streams: bool, fused: bool = False) -> int:
 # scaled x8 (experts and tokens) and the shared expert's weights are not
 # (profiles/grouped_gemm_tc_dsv3_prefill_e32.md).  Reported as null once the
 # kernel source no longer matches the captured one.
-TRAFFIC = {"source_sha256": "43f0c4a3734291ddb3595305f1c70d1b295cdbc48832ba922349073bbe4badb9",
-           # routed gate/up launch (the shared expert runs on the second
-           # stream): dsv3_prefill from a one-pass capture of the full layer,
-           # dsv3_prefill_e32 from a capture of the 32-expert case
-           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.969214e9,
-                                            "dsv3_prefill": 15.820377e9}}
+TRAFFIC = {"source_sha256": "5117257942e3696d4f246a3e4945a4dd18c565d1f30aa2e30d33d5b655116473",
+           # routed gate/up launch on tile-major weights (the shared expert
+           # runs on the second stream): dsv3_prefill from a one-pass capture
+           # of the full layer, dsv3_prefill_e32 from a capture of the
+           # 32-expert case
+           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.969278e9,
+                                            "dsv3_prefill": 15.827366e9}}
 
 
 def peaks():
