@@ -34,13 +34,13 @@ UNIT = "tokens/s"
 L2_FLUSH_BYTES = 512 << 20
 
 
-def launches_per_step(cfg, two_streams: bool, fused: bool = False) -> int:
+def launches_per_step(cfg, two_streams: bool, fused: bool = False, presplit: bool = False) -> int:
     """Our kernels per moe_layer call."""
     n = 4  # top-k, count+scan, permute, router GEMM
     if not fused:
         n += 1  # combine
-    if cfg.dtype == "bf16":
-        n += 1  # router weight split
+    if cfg.dtype == "bf16" and not presplit:
+        n += 1  # router weight split (unless made once beforehand)
     n += 2  # gate/up and down grouped GEMMs (routed)
     if cfg.shared_I:
         if cfg.dtype == "bf16" and cfg.shared_I == cfg.I and (not two_streams or fused):
@@ -523,7 +523,8 @@ def run_ours(args, cfg):
         cpu = cpu_baseline(cfg, inp)
 
     if rank == 0:
-        launches = launches_per_step(cfg, two_streams, args.fused_combine) * K
+        launches = launches_per_step(cfg, two_streams, args.fused_combine,
+                                     layer.w_router_split is not None) * K
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": warm, "ms_per_step": 1e3 * total_s / K, "higher_is_better": True,

@@ -27,7 +27,7 @@ SYMBOLS = ("moe_status_string", "moe_version", "moe_route_from_scores", "moe_rou
            "moe_dispatch_workspace_size", "moe_dispatch", "moe_grouped_ffn_workspace_size",
            "moe_grouped_ffn", "moe_combine", "moe_layer_workspace_size", "moe_layer",
            "moe_check_error", "moe_dispatch_noalloc", "moe_selftest_bounded_wait",
-           "moe_pack_expert_weights")
+           "moe_pack_expert_weights", "moe_split_router_weight")
 
 
 class MoEError(RuntimeError):
@@ -50,7 +50,7 @@ class LayerArgs(ctypes.Structure):
                 ("route", RouteCfg), ("scores_out", ctypes.c_void_p),
                 ("topk_idx_out", ctypes.c_void_p), ("topk_w_out", ctypes.c_void_p),
                 ("offsets_out", ctypes.c_void_p), ("stage_events", ctypes.c_void_p),
-                ("flags", ctypes.c_int32)]
+                ("flags", ctypes.c_int32), ("w_router_split", ctypes.c_void_p)]
 
 LAYER_FUSED_COMBINE = 1
 LAYER_PACKED_WEIGHTS = 2
@@ -103,6 +103,8 @@ def load() -> ctypes.CDLL:
     lib.moe_selftest_bounded_wait.restype = i32
     lib.moe_pack_expert_weights.argtypes = [P, P, i32, i32, i32, P, P, P]
     lib.moe_pack_expert_weights.restype = i32
+    lib.moe_split_router_weight.argtypes = [P, i32, i32, P, P]
+    lib.moe_split_router_weight.restype = i32
     _lib = lib
     return lib
 
@@ -252,9 +254,10 @@ def moe_combine(y_perm, slot_to_row, topk_w, shared, out, stream=None):
 
 def layer_args(x, w_router, bias, w13, w2, w13_sh, w2_sh, cfg: RouteCfg, scores_out=None,
                topk_idx_out=None, topk_w_out=None, offsets_out=None,
-               stage_events=None, flags: int = 0) -> LayerArgs:
+               stage_events=None, flags: int = 0, w_router_split=None) -> LayerArgs:
     """``stage_events``: None or a list of LAYER_EVENTS torch.cuda.Event (kept
-    alive by the caller), recorded by the library at the stage boundaries."""
+    alive by the caller), recorded by the library at the stage boundaries.
+    ``w_router_split``: the router weight from moe_split_router_weight, or None."""
     T, d = x.shape
     I = w2.shape[2]
     I_sh = w2_sh.shape[1] if w2_sh is not None else 0
@@ -265,7 +268,8 @@ def layer_args(x, w_router, bias, w13, w2, w13_sh, w2_sh, cfg: RouteCfg, scores_
                      _ptr(scores_out, torch.float32, "scores_out"),
                      _ptr(topk_idx_out, torch.int32, "topk_idx_out"),
                      _ptr(topk_w_out, torch.float32, "topk_w_out"),
-                     _ptr(offsets_out, torch.int32, "offsets_out"), _events(stage_events), flags)
+                     _ptr(offsets_out, torch.int32, "offsets_out"), _events(stage_events), flags,
+                     _ptr(w_router_split, torch.bfloat16, "w_router_split"))
 
 
 _event_arrays = {}
@@ -343,6 +347,18 @@ def moe_pack_expert_weights(w13, w2, w13_packed, w2_packed, stream=None):
     _check(rc, "moe_pack_expert_weights")
 
 
+def moe_split_router_weight(w_router, out=None, stream=None):
+    """w_router [E,d] fp32 -> [3,E,d] bf16 (hi, mid, lo), the router's tensor-core
+    operand, for LayerArgs.w_router_split.  Returns ``out``."""
+    E, d = w_router.shape
+    if out is None:
+        out = torch.empty((3, E, d), dtype=torch.bfloat16, device=w_router.device)
+    rc = load().moe_split_router_weight(_ptr(w_router, torch.float32, "w_router"), E, d,
+                                        _ptr(out, torch.bfloat16, "out"), _stream(stream))
+    _check(rc, "moe_split_router_weight")
+    return out
+
+
 def packable(w13, w2, w13_sh=None, w2_sh=None) -> bool:
     """Whether the tile-major layouts apply (bf16, I % 128 == 0, d % 256 == 0)."""
     if w13.dtype != torch.bfloat16:
@@ -363,7 +379,8 @@ class MoELayer:
     """
 
     def __init__(self, w_router, bias, w13, w2, w13_sh, w2_sh, cfg: RouteCfg, T: int,
-                 overlap: bool = True, fused_combine: bool = False, pack_weights: bool = True):
+                 overlap: bool = True, fused_combine: bool = False, pack_weights: bool = True,
+                 split_router: bool = True):
         self.cfg = cfg
         self.T = T
         dev = w13.device
@@ -381,6 +398,10 @@ class MoELayer:
                 w13_sh, w2_sh = p13s, p2s
             self.flags |= LAYER_PACKED_WEIGHTS
         self.w = dict(w_router=w_router, bias=bias, w13=w13, w2=w2, w13_sh=w13_sh, w2_sh=w2_sh)
+        # the bf16 router multiplies a three-term split of its fp32 weight:
+        # made once here instead of on every call
+        self.w_router_split = (moe_split_router_weight(w_router)
+                               if split_router and w13.dtype == torch.bfloat16 else None)
         sizes = LayerArgs(None, None, None, None, None, None, None, T, d, w2.shape[2], I_sh,
                           _dtype_code(w13), cfg, None, None, None, None, None, self.flags)
         self.ws_bytes = moe_layer_workspace_size(sizes)
@@ -390,7 +411,8 @@ class MoELayer:
     def _args(self, x, **outs):
         w = self.w
         return layer_args(x, w["w_router"], w["bias"], w["w13"], w["w2"], w["w13_sh"],
-                          w["w2_sh"], self.cfg, flags=self.flags, **outs)
+                          w["w2_sh"], self.cfg, flags=self.flags,
+                          w_router_split=self.w_router_split, **outs)
 
     def forward(self, x, out=None, stream=None, **outs):
         """out [T,d] fp32 for x [T,d] (device tensors), enqueued on `stream`

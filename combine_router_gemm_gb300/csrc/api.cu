@@ -101,13 +101,14 @@ size_t route_ws(int T, int E, int d, int dtype) {
 // work); fp32, after the router GEMM.
 int run_route(const void* x, int dtype, const float* w_router, const float* bias, int T, int d,
               const moe_route_cfg* cfg, float* scores, int32_t* idx, float* w, void* rws,
-              uint32_t* err, unsigned* work, cudaStream_t s, cudaEvent_t side_start = nullptr) {
+              uint32_t* err, unsigned* work, cudaStream_t s, cudaEvent_t side_start = nullptr,
+              const void* presplit = nullptr) {
     const int E = cfg->num_experts;
     if (dtype == MOE_BF16) {
         float* partial = nullptr;
         int ks = 0;
         int rc = moe_tc::router_bf16(x, w_router, T, d, E, rws, err, work, &partial, &ks, s,
-                                     side_start);
+                                     side_start, presplit);
         if (rc != MOE_OK) return rc;
         return moe_launch::topk(nullptr, bias, T, cfg, idx, w, s, partial, ks, scores);
     }
@@ -195,6 +196,9 @@ int check_layer(const moe_layer_args* a) {
         if (!moe_host::aligned16(a->w13_sh) || !moe_host::aligned16(a->w2_sh))
             return MOE_ERR_INVALID_ARG;
     }
+    if (a->w_router_split &&
+        (a->dtype != MOE_BF16 || !moe_host::aligned16(a->w_router_split)))
+        return MOE_ERR_INVALID_ARG;
     const void* outs[] = {a->scores_out, a->topk_idx_out, a->topk_w_out, a->offsets_out};
     for (const void* o : outs)
         if (o && !moe_host::aligned16(o)) return MOE_ERR_INVALID_ARG;
@@ -390,7 +394,8 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     // down tiles in the routed down launch: 4.057 vs 4.110 ms.
     if (rc == MOE_OK)
         rc = run_route(a->x, a->dtype, a->w_router, a->bias, T, d, &a->route, w.scores, w.idx, w.w,
-                       w.wsplit, w.err, ctr(w.err, CTR_ROUTER), s0, overlap ? ev_start : nullptr);
+                       w.wsplit, w.err, ctr(w.err, CTR_ROUTER), s0, overlap ? ev_start : nullptr,
+                       a->w_router_split);
     mark(1);
     mark(2);
     const bool fused = a->flags & MOE_LAYER_FUSED_COMBINE;
@@ -445,6 +450,12 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     if (ev_start) cudaEventDestroy(ev_start);
     if (ev_shared) cudaEventDestroy(ev_shared);
     return rc;
+}
+
+int moe_split_router_weight(const float* w_router, int E, int d, void* out, void* stream) {
+    if (E < 1 || d < 8 || d % 8 != 0 || !w_router || !out) return MOE_ERR_INVALID_ARG;
+    if (!moe_host::aligned16(w_router) || !moe_host::aligned16(out)) return MOE_ERR_INVALID_ARG;
+    return moe_tc::split_router_weight(w_router, E, d, out, static_cast<cudaStream_t>(stream));
 }
 
 int moe_pack_expert_weights(const void* w13, const void* w2, int E, int d, int I,

@@ -93,10 +93,14 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
 int pack_weights(const void* w, int E, int rows, int K, bool pairs, void* out, cudaStream_t s);
 size_t router_ws_bytes(int T, int E, int d);
 int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s);
-// after_split: recorded once the weight split is done, before the GEMM
+// after_split: recorded once the weight split is done, before the GEMM.
+// presplit: the weight already split ([3,E,d] bf16), or NULL to split it
+// into the workspace first.
 int router_bf16(const void* x, const float* w_router, int T, int d, int E, void* ws,
                 uint32_t* err, unsigned* work, float** partial, int* ksplit, cudaStream_t s,
-                cudaEvent_t after_split = nullptr);
+                cudaEvent_t after_split = nullptr, const void* presplit = nullptr);
+// w_router [E,d] fp32 -> out [3,E,d] bf16 (hi, mid, lo), on stream s
+int split_router_weight(const float* w_router, int E, int d, void* out, cudaStream_t s);
 }  // namespace moe_tc
 
 // ---- internal launchers (one per kernel family), used by api.cu -----------

@@ -848,7 +848,8 @@ __global__ void mbar_probe_kernel(uint64_t limit_ns, uint32_t* err) {
 }
 
 // Router weight split: w = hi + mid + lo with each term the bf16 rounding of
-// what the previous terms leave (every subtraction is exact in fp32).
+// what the previous terms leave (every subtraction is exact in fp32; the sum
+// is exact for |w| >= 2^-110, below which bf16's spacing drops the last bits).
 __global__ void split_weight_kernel(const float* __restrict__ w, long n,
                                     __nv_bfloat16* __restrict__ out) {
     for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n;
@@ -1070,17 +1071,24 @@ size_t router_ws_bytes(int T, int E, int d) {
 // Partial logits of x W^T (fp32 accumulate) with W split into three bf16
 // terms: K is cut into *ksplit parts (chosen so that the units fill the SMs),
 // part ks written to partial + ks * T * E.  ws: router_ws_bytes(T, E, d).
-int router_bf16(const void* x, const float* w_router, int T, int d, int E, void* ws,
-                uint32_t* err, unsigned* work, float** partial, int* ksplit, cudaStream_t s,
-                cudaEvent_t after_split) {
-    __nv_bfloat16* wsplit = static_cast<__nv_bfloat16*>(ws);
-    const size_t split = ((size_t)3 * E * d * 2 + 255) / 256 * 256;
-    float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + split);
+int split_router_weight(const float* w_router, int E, int d, void* out, cudaStream_t s) {
     const long n = (long)E * d;
     const int blocks = (int)std::min<long>((n + 255) / 256, 4L * moe_host::num_sms());
-    split_weight_kernel<<<blocks, 256, 0, s>>>(w_router, n, wsplit);
-    int rc = moe_host::launch_status();
-    if (rc != MOE_OK) return rc;
+    split_weight_kernel<<<blocks, 256, 0, s>>>(w_router, n, static_cast<__nv_bfloat16*>(out));
+    return moe_host::launch_status();
+}
+
+int router_bf16(const void* x, const float* w_router, int T, int d, int E, void* ws,
+                uint32_t* err, unsigned* work, float** partial, int* ksplit, cudaStream_t s,
+                cudaEvent_t after_split, const void* presplit) {
+    const size_t split = ((size_t)3 * E * d * 2 + 255) / 256 * 256;
+    float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + split);
+    const void* wsplit = presplit;
+    if (!wsplit) {
+        wsplit = ws;
+        const int rc = split_router_weight(w_router, E, d, ws, s);
+        if (rc != MOE_OK) return rc;
+    }
     if (after_split && cudaEventRecord(after_split, s) != cudaSuccess) return MOE_ERR_CUDA;
     CUtensorMap a;
     BMaps b;

@@ -193,6 +193,9 @@ typedef struct {
     int32_t* offsets_out;   /* [E+1]  or NULL */
     void* const* stage_events; /* MOE_LAYER_EVENTS cudaEvent_t, or NULL */
     int32_t flags;          /* MOE_LAYER_* bits, 0 = defaults */
+    /* bf16 only, optional: w_router already split by moe_split_router_weight
+     * ([3,E,d] bf16), so that the call skips that step; NULL: split per call */
+    const void* w_router_split;
 } moe_layer_args;
 
 /* moe_layer_args.flags: add the down projection's results straight into `out`
@@ -244,6 +247,15 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
  *   inputs.  Asynchronous on `stream`. */
 int moe_pack_expert_weights(const void* w13, const void* w2, int E, int d, int I,
                             void* w13_packed, void* w2_packed, void* stream);
+
+/* The fp32 router weight [E,d] as the three bf16 terms the tensor-core router
+ * multiplies (out [3,E,d] bf16: hi, mid, lo, each term the bf16 rounding of
+ * what the previous ones leave; w = hi + mid + lo exactly for |w| >= 2^-110,
+ * to within 2^-134 below, where bf16's finest spacing ends), for
+ * moe_layer_args.w_router_split: a one-time preparation instead of a split
+ * on every call.  E >= 1, d >= 8 with d % 8 == 0, 16-byte aligned device
+ * pointers (MOE_ERR_INVALID_ARG otherwise).  Asynchronous on `stream`. */
+int moe_split_router_weight(const float* w_router, int E, int d, void* out, void* stream);
 
 /* ------------------------------------------------- allocation-free dispatch */
 

@@ -169,3 +169,21 @@ def test_layer_packed_flag_checks(lib):
         n = lib.moe_layer_workspace_size(ctypes.byref(a)) or need
         assert lib.moe_layer(ctypes.byref(a), P, P, n, None, None) == B.ERR_UNSUPPORTED, bad
     assert lib.moe_layer(ctypes.byref(args(flags=8)), P, P, need, None, None) == B.ERR_INVALID_ARG
+
+
+def test_split_router_weight_rejects(lib):
+    assert lib.moe_split_router_weight(P, 0, 64, P, None) == B.ERR_INVALID_ARG
+    assert lib.moe_split_router_weight(P, 8, 60, P, None) == B.ERR_INVALID_ARG
+    assert lib.moe_split_router_weight(None, 8, 64, P, None) == B.ERR_INVALID_ARG
+    assert lib.moe_split_router_weight(P, 8, 64, P + 4, None) == B.ERR_INVALID_ARG
+
+
+def test_layer_presplit_router_checks(lib):
+    a = B.LayerArgs(x=P, w_router=P, w13=P, w2=P, T=64, d=128, I=256, dtype=B.F32,
+                    route=cfg(), w_router_split=P)
+    need = lib.moe_layer_workspace_size(ctypes.byref(a))
+    # an fp32 layer has no split router weight
+    assert lib.moe_layer(ctypes.byref(a), P, P, need, None, None) == B.ERR_INVALID_ARG
+    a.dtype, a.w_router_split = B.BF16, P + 8
+    need = lib.moe_layer_workspace_size(ctypes.byref(a))
+    assert lib.moe_layer(ctypes.byref(a), P, P, need, None, None) == B.ERR_INVALID_ARG

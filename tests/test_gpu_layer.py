@@ -294,3 +294,18 @@ def test_layer_packed_weights_bit_identical(overlap):
     for layer in (packed, plain):
         rc, detail = B.moe_check_error(layer.ws)
         assert rc == B.OK, detail
+
+
+def test_layer_presplit_router_bit_identical():
+    """The router weight split once beforehand gives the same layer output,
+    bit for bit, as splitting it on every call."""
+    cfg = SMALL_BF16[0]
+    inp = inputs.make_inputs(cfg, seed=9, device="cuda")
+    args = (inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"], inp["w2_sh"],
+            B.cfg_from(cfg), cfg.T)
+    once = B.MoELayer(*args, split_router=True)
+    each = B.MoELayer(*args, split_router=False)
+    assert once.w_router_split is not None and each.w_router_split is None
+    a, b = once.forward(inp["x"]), each.forward(inp["x"])
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)

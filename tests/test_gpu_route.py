@@ -115,3 +115,27 @@ def test_router_tensor_core_split_weight(oracle, T, d, E, fn):
     ofn = oracle.SIGMOID if fn == "sigmoid" else oracle.SOFTMAX
     ref = oracle.router_scores(np_(x), np_(wr), ofn)
     np.testing.assert_allclose(np_(scores), ref, rtol=1e-6, atol=tc_router_atol(d))
+
+
+def test_split_router_weight_terms_sum_exactly():
+    """hi + mid + lo reproduces every fp32 router weight of magnitude >= 2^-110
+    exactly (smaller ones to within 2^-134), each term is bf16, and the terms
+    shrink by at least 2^8 each."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    w = torch.randn((256, 7168), generator=g, device="cuda") * 0.02
+    w[0, :7] = torch.tensor([0.0, -0.0, 1.0, -3.5, 1e-30, 3.0e38, 2.0 ** -126], device="cuda")
+    # an fp32 subnormal with bits below bf16's finest spacing (2^-133)
+    w[0, 7] = 2.0 ** -126 / 3
+    sp = B.moe_split_router_weight(w)
+    torch.cuda.synchronize()
+    assert sp.dtype == torch.bfloat16 and sp.shape == (3, 256, 7168)
+    terms = sp.double()
+    total, ref = terms.sum(0), w.double()
+    exact = torch.ones_like(ref, dtype=torch.bool)
+    exact[0, 7] = False
+    assert torch.equal(total[exact], ref[exact])
+    assert (total[0, 7] - ref[0, 7]).abs() <= 2.0 ** -134
+    hi, mid, lo = terms
+    assert (mid.abs() <= hi.abs() * 2.0 ** -8 + 1e-45).all()
+    assert (lo.abs() <= mid.abs() * 2.0 ** -8 + 1e-45).all()
