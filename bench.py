@@ -57,13 +57,13 @@ def launches_per_step(cfg, two_streams: bool, fused: bool = False, presplit: boo
 # scaled x8 (experts and tokens) and the shared expert's weights are not
 # (profiles/grouped_gemm_tc_dsv3_prefill_e32.md).  Reported as null once the
 # kernel source no longer matches the captured one.
-TRAFFIC = {"source_sha256": "5117257942e3696d4f246a3e4945a4dd18c565d1f30aa2e30d33d5b655116473",
+TRAFFIC = {"source_sha256": "2fa131f32e04477848d0b763103c9eece876dd7f1e4f0bdc14a7a607a44d91fa",
            # routed gate/up launch on tile-major weights (the shared expert
            # runs on the second stream): dsv3_prefill from a one-pass capture
            # of the full layer, dsv3_prefill_e32 from a capture of the
            # 32-expert case
-           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.969278e9,
-                                            "dsv3_prefill": 15.827366e9}}
+           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.969362e9,
+                                            "dsv3_prefill": 15.822849e9}}
 
 
 def peaks():
