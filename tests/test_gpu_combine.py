@@ -47,3 +47,22 @@ def test_combine_identity_experts(oracle):
     B.moe_combine(y, s2r, w, None, out)
     ref = w.double().sum(1, keepdim=True) * x.double()
     np.testing.assert_allclose(np_(out), np_(ref), rtol=1e-6, atol=1e-6)
+
+
+def test_combine_out_of_range_row_is_visible():
+    """A slot_to_row entry outside y poisons that token's output row (NaN) and
+    no other; nothing outside y is read."""
+    T, k, d = 64, 8, 256
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4)
+    y = torch.randn((T * k, d), generator=g, device="cuda")
+    w = torch.rand((T, k), generator=g, device="cuda")
+    s2r = perm_maps(T, k, 5).cuda()
+    s2r[3 * k + 2] = T * k + 7  # token 3, slot 2
+    s2r[9 * k] = -1             # token 9, slot 0
+    out = cuda_f32((T, d))
+    B.moe_combine(y, s2r, w, None, out)
+    torch.cuda.synchronize()
+    bad = torch.isnan(out).any(1)
+    assert bad[3] and bad[9]
+    assert not bad[[t for t in range(T) if t not in (3, 9)]].any()
