@@ -138,3 +138,20 @@ def test_pack_expert_weights_layout(E, d, I):
     torch.cuda.synchronize()
     assert torch.equal(s13, torch_pack(w13[0], False))
     assert torch.equal(s2, torch_pack(w2[0], True))
+
+
+def test_grouped_ffn_bf16_mixed_classes_wide_tiles(oracle):
+    """Many experts, 256-row token tiles (at least 384 rows per expert on
+    average): compute-class experts (at least 128 rows) interleaved with
+    weight-streaming ones of ragged sizes, empty experts between them."""
+    E, d, I = 64, 256, 128
+    rng = np.random.default_rng(5)
+    counts = [2300] * 10 + [int(c) for c in rng.integers(1, 128, 40)] + [0] * 14
+    counts = [counts[i] for i in rng.permutation(E)]
+    assert sum(counts) >= 384 * E  # the wide-tile launch configuration
+    x, offsets, w13, w2 = make_case(E, d, I, counts, torch.bfloat16, seed=77)
+    y = run_ffn(x, offsets, w13, w2)
+    torch.cuda.synchronize()
+    n = int(offsets[-1])
+    ref = oracle.grouped_ffn(np_(x), np_(offsets), np_(w13), np_(w2), round_h=True)
+    assert_bf16_close(np_(y)[:n], ref, "mixed classes")
