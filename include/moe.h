@@ -145,7 +145,7 @@ size_t moe_grouped_ffn_workspace_size(int rows, int d, int I, int dtype);
  *   H[r]  = silu(x_perm[r] W1_e^T) * (x_perm[r] W3_e^T)   (bf16 for bf16)
  *   y[r]  = H[r] W2_e^T                                     (fp32)
  *   w13 [E,2I,d]: rows 0..I-1 are W1 (gate), rows I..2I-1 are W3 (up)
- *   w2  [E,d,I]
+ *   w2  [E,d,I]   (row-major; the tile-major layouts are for moe_layer)
  *   x_perm [rows,d], y_perm [rows,d] fp32 (rows past offsets[E] untouched).
  * bf16 runs on the tcgen05 tensor cores with fp32 accumulation; fp32 runs on
  * the CUDA cores in fp32.  Experts with no rows read none of their weights.
