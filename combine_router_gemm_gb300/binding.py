@@ -54,6 +54,7 @@ class LayerArgs(ctypes.Structure):
 
 LAYER_FUSED_COMBINE = 1
 LAYER_PACKED_WEIGHTS = 2
+LAYER_SHARED_AFTER_ROUTER = 4
 
 LAYER_EVENTS = 7
 
@@ -398,6 +399,7 @@ class MoELayer:
                 w13_sh, w2_sh = p13s, p2s
             self.flags |= LAYER_PACKED_WEIGHTS
         self.w = dict(w_router=w_router, bias=bias, w13=w13, w2=w2, w13_sh=w13_sh, w2_sh=w2_sh)
+        self._extra_flags = 0
         # the bf16 router multiplies a three-term split of its fp32 weight:
         # made once here instead of on every call
         self.w_router_split = (moe_split_router_weight(w_router)
@@ -411,7 +413,7 @@ class MoELayer:
     def _args(self, x, **outs):
         w = self.w
         return layer_args(x, w["w_router"], w["bias"], w["w13"], w["w2"], w["w13_sh"],
-                          w["w2_sh"], self.cfg, flags=self.flags,
+                          w["w2_sh"], self.cfg, flags=self.flags | self._extra_flags,
                           w_router_split=self.w_router_split, **outs)
 
     def forward(self, x, out=None, stream=None, **outs):
@@ -424,7 +426,7 @@ class MoELayer:
         moe_layer(self._args(x, **outs), out, self.ws, stream=stream, stream2=self.stream2)
         return out
 
-    def capture(self, x, out=None, **outs):
+    def capture(self, x, out=None, shared_after_router: bool = True, **outs):
         """Record one ``forward(x)`` into a CUDA graph and return ``(graph,
         out)``.
 
@@ -433,7 +435,9 @@ class MoELayer:
         ``out``; the optional outputs (``scores_out`` ...) are static as well.
         One call runs first, outside the capture, so that the per-device
         kernel settings are made before capturing.  The second stream of the
-        layer is forked from and joined back into the capture by events.
+        layer is forked from and joined back into the capture by events; with
+        ``shared_after_router`` its work follows the router GEMM in the graph
+        (LAYER_SHARED_AFTER_ROUTER), a fixed order that replays keep.
         """
         if out is None:
             out = torch.empty((x.shape[0], x.shape[1]), dtype=torch.float32, device=x.device)
@@ -444,8 +448,12 @@ class MoELayer:
             self.forward(x, out=out, **outs)
         torch.cuda.current_stream(dev).wait_stream(side)
         graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, capture_error_mode="relaxed"):
-            self.forward(x, out=out, **outs)
+        self._extra_flags = LAYER_SHARED_AFTER_ROUTER if shared_after_router else 0
+        try:
+            with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+                self.forward(x, out=out, **outs)
+        finally:
+            self._extra_flags = 0
         return graph, out
 
     def forward_host(self, host_inputs, host_outputs):

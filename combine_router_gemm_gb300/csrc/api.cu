@@ -98,18 +98,21 @@ size_t route_ws(int T, int E, int d, int dtype) {
 // side_start (optional) is recorded where work on another stream may begin:
 // bf16, once the router weight is split (the router GEMM is one wave that
 // leaves SMs idle, and the top-k and dispatch kernels share SMs with other
-// work); fp32, after the router GEMM.
+// work), or with side_after_gemm after the router GEMM; fp32, after the
+// router GEMM.
 int run_route(const void* x, int dtype, const float* w_router, const float* bias, int T, int d,
               const moe_route_cfg* cfg, float* scores, int32_t* idx, float* w, void* rws,
               uint32_t* err, unsigned* work, cudaStream_t s, cudaEvent_t side_start = nullptr,
-              const void* presplit = nullptr) {
+              const void* presplit = nullptr, bool side_after_gemm = false) {
     const int E = cfg->num_experts;
     if (dtype == MOE_BF16) {
         float* partial = nullptr;
         int ks = 0;
         int rc = moe_tc::router_bf16(x, w_router, T, d, E, rws, err, work, &partial, &ks, s,
-                                     side_start, presplit);
+                                     side_after_gemm ? nullptr : side_start, presplit);
         if (rc != MOE_OK) return rc;
+        if (side_after_gemm && side_start && cudaEventRecord(side_start, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
         return moe_launch::topk(nullptr, bias, T, cfg, idx, w, s, partial, ks, scores);
     }
     int rc = moe_launch::router_gemm(x, dtype, w_router, T, d, E, cfg->score_fn, scores, s);
@@ -202,7 +205,9 @@ int check_layer(const moe_layer_args* a) {
     const void* outs[] = {a->scores_out, a->topk_idx_out, a->topk_w_out, a->offsets_out};
     for (const void* o : outs)
         if (o && !moe_host::aligned16(o)) return MOE_ERR_INVALID_ARG;
-    if (a->flags & ~(MOE_LAYER_FUSED_COMBINE | MOE_LAYER_PACKED_WEIGHTS)) return MOE_ERR_INVALID_ARG;
+    if (a->flags & ~(MOE_LAYER_FUSED_COMBINE | MOE_LAYER_PACKED_WEIGHTS |
+                     MOE_LAYER_SHARED_AFTER_ROUTER))
+        return MOE_ERR_INVALID_ARG;
     if ((a->flags & MOE_LAYER_PACKED_WEIGHTS) &&
         (a->dtype != MOE_BF16 || a->I % 128 != 0 || a->d % 256 != 0 || a->I_sh % 128 != 0))
         return MOE_ERR_UNSUPPORTED;
@@ -395,7 +400,7 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     if (rc == MOE_OK)
         rc = run_route(a->x, a->dtype, a->w_router, a->bias, T, d, &a->route, w.scores, w.idx, w.w,
                        w.wsplit, w.err, ctr(w.err, CTR_ROUTER), s0, overlap ? ev_start : nullptr,
-                       a->w_router_split);
+                       a->w_router_split, a->flags & MOE_LAYER_SHARED_AFTER_ROUTER);
     mark(1);
     mark(2);
     const bool fused = a->flags & MOE_LAYER_FUSED_COMBINE;

@@ -212,6 +212,13 @@ typedef struct {
  * the row-major weights they were packed from. */
 #define MOE_LAYER_PACKED_WEIGHTS 2
 
+/* moe_layer_args.flags: the shared expert's work on stream2 starts once the
+ * router GEMM has finished, rather than when it is launched.  A fixed order
+ * for CUDA-graph capture: a replayed graph may otherwise start the shared
+ * expert's first GEMM ahead of the router GEMM and delay it.  Results are
+ * the same either way. */
+#define MOE_LAYER_SHARED_AFTER_ROUTER 4
+
 /* Workspace bytes moe_layer needs (0 for invalid sizes or configuration).
  * Only the sizes, dtype, routing configuration, I_sh (> 0: shared expert
  * present) and which optional outputs are non-NULL matter here; the input

@@ -187,3 +187,10 @@ def test_layer_presplit_router_checks(lib):
     a.dtype, a.w_router_split = B.BF16, P + 8
     need = lib.moe_layer_workspace_size(ctypes.byref(a))
     assert lib.moe_layer(ctypes.byref(a), P, P, need, None, None) == B.ERR_INVALID_ARG
+
+
+def test_layer_flag_bits(lib):
+    a = B.LayerArgs(x=P, w_router=P, w13=P, w2=P, T=64, d=128, I=256, dtype=B.F32, route=cfg(),
+                    flags=B.LAYER_SHARED_AFTER_ROUTER | 16)
+    need = lib.moe_layer_workspace_size(ctypes.byref(a))
+    assert lib.moe_layer(ctypes.byref(a), P, P, need, None, None) == B.ERR_INVALID_ARG
