@@ -51,15 +51,14 @@ def launches_per_step(cfg, two_streams: bool, fused: bool = False, presplit: boo
             n += 2  # its own two launches
     return n
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the routed
-# (+ shared) gate/up GEMM per launch, from one ncu capture of this kernel
-# source on the 32-expert workload; at the 256-expert layer the routed part is
-# scaled x8 (experts and tokens) and the shared expert's weights are not
-# (profiles/grouped_gemm_tc_dsv3_prefill_e32.md).  Reported as null once the
-# kernel source no longer matches the captured one.
+# nominal GB300 peaks, quoted beside the measured ones for context
 NOMINAL_HBM_GBS = 7900.0
 NOMINAL_BF16_TFLOPS = 2250.0
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the routed
+# gate/up GEMM per launch, from ncu captures of this kernel source
+# (profiles/grouped_gemm_tc_dsv3_prefill_dram.md, ..._e32.md).  Reported as
+# null once the kernel source no longer matches the captured one.
 TRAFFIC = {"source_sha256": "2fa131f32e04477848d0b763103c9eece876dd7f1e4f0bdc14a7a607a44d91fa",
            # routed gate/up launch on tile-major weights (the shared expert
            # runs on the second stream): dsv3_prefill from a one-pass capture
