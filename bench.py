@@ -246,6 +246,25 @@ def eager_layer(cfg, inp):
     return out
 
 
+def dispatch_alone_ms(cfg, x, layer, flush, steps=20):
+    """moe_dispatch (histogram, scan, permute) timed on its own, on the
+    routing of the layer's input (L2 flushed before each call)."""
+    import torch
+    from combine_router_gemm_gb300 import binding as B
+    S = cfg.S
+    idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device="cuda")
+    layer.forward(x, topk_idx_out=idx)
+    counts = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(cfg.E + 1, dtype=torch.int32, device="cuda")
+    s2r = torch.empty(S, dtype=torch.int32, device="cuda")
+    r2t = torch.empty(S, dtype=torch.int32, device="cuda")
+    xp = torch.empty((S, cfg.d), dtype=x.dtype, device="cuda")
+    ws = torch.empty(B.moe_dispatch_workspace_size(cfg.T, cfg.k, cfg.E), dtype=torch.uint8,
+                     device="cuda")
+    return time_cuda(lambda: B.moe_dispatch(idx, x, cfg.E, counts, offsets, s2r, r2t, xp, ws),
+                     steps, flush)
+
+
 def time_cuda(fn, steps, flush):
     import torch
     fn()
@@ -467,7 +486,12 @@ def run_ours(args, cfg):
         return f / (ms * 1e-3) / 1e12
 
     stages["dispatch"].update(GBps=round(bw(perm_bytes, stage_ms[2]), 1),
-                              frac_hbm=round(bw(perm_bytes, stage_ms[2]) / pk["hbm_gbs"], 4))
+                              frac_hbm=round(bw(perm_bytes, stage_ms[2]) / pk["hbm_gbs"], 4),
+                              note="count + permute, beside the shared expert's GEMMs")
+    # the dispatch (count + permute) alone, on this step's routing
+    d_ms = dispatch_alone_ms(cfg, x, layer, flush, steps=min(K, 20))
+    stages["dispatch_alone"] = {"ms": round(d_ms, 4), "GBps": round(bw(perm_bytes, d_ms), 1),
+                                "frac_hbm": round(bw(perm_bytes, d_ms) / pk["hbm_gbs"], 4)}
     for key, b, f, ms in (("gate_up_gemm", gu_bytes, gu_flops, stage_ms[3]),
                           ("down_gemm", dn_bytes, dn_flops, stage_ms[4])):
         stages[key].update(GBps=round(bw(b, ms), 1), TFLOPs=round(tf(f, ms), 1),
