@@ -10,9 +10,16 @@
 // GPU that loads the library holds it until the process exits.
 //
 // Host code must not use the array's name as a device address (on the host it
-// names a host-side stand-in).  The device address is looked up once per
-// device with cudaGetSymbolAddress, with that device current, on the first
-// call made on that device, and cached.
+// names a host-side stand-in).  The device address is looked up with
+// cudaGetSymbolAddress, with the device current, on the first call made on
+// that device, and cached together with the identity of the CUDA context it
+// was looked up in.  If that context is later replaced (cudaDeviceReset, or
+// the primary context released and created again), the module is loaded
+// anew and the array may move: the next call sees a different context and
+// looks the address up again instead of using a stale one.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -28,20 +35,55 @@ constexpr int MAX_DEVICES = 64;
 static __device__ __align__(256) unsigned char g_dispatch_scratch[NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_mu;
-void* g_scratch_addr[MAX_DEVICES] = {};
+struct CachedAddr {
+    unsigned long long ctx_id;  // context the address belongs to (0 = none yet)
+    void* addr;
+};
+CachedAddr g_scratch_addr[MAX_DEVICES] = {};
 
-// Device address of the scratch array on the current device (set-up on first
-// use per device).  Returns nullptr if the lookup fails.
+// Unique id of the calling thread's current CUDA context (driver API through
+// the runtime's entry-point query; context ids are never reused, unlike
+// context handles).  Returns false if there is no current context.
+bool current_context_id(unsigned long long* id) {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static bool resolved = false;
+    if (!resolved) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+        resolved = true;
+    }
+    if (!get_current || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current device's current
+// context: looked up on the first call per device, and again whenever the
+// context has changed since.  Returns nullptr if the lookup fails.
 void* scratch_address() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return nullptr;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess) return nullptr;
-        g_scratch_addr[dev] = p;
-    }
-    return g_scratch_addr[dev];
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
+    CachedAddr& c = g_scratch_addr[dev];
+    if (have_id && c.addr && c.ctx_id == id) return c.addr;
+    void* p = nullptr;
+    // (creates the device's primary context first if the thread has none)
+    if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess) return nullptr;
+    if (!have_id && !current_context_id(&id)) id = 0;  // no id: not cached
+    c.ctx_id = id;
+    c.addr = id ? p : nullptr;
+    return p;
 }
 
 }  // namespace
