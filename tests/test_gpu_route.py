@@ -9,7 +9,7 @@ import torch
 
 from combine_router_gemm_gb300 import binding as B
 from combine_router_gemm_gb300 import inputs
-from helpers import GATE_RTOL, cuda_f32, cuda_i32, near_tie_tokens, np_, tc_router_atol
+from helpers import GATE_RTOL, cuda_f32, cuda_i32, near_tie_tokens, np_, tc_router_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -85,14 +85,27 @@ def test_route_full_router(oracle, name):
     torch.cuda.synchronize()
     fn = oracle.SIGMOID if cfg.score_fn == "sigmoid" else oracle.SOFTMAX
     ref_sc = oracle.router_scores(np_(inp["x"]), np_(inp["w_router"]), fn)
-    atol = tc_router_atol(cfg.d) if cfg.dtype == "bf16" else 2e-5
-    np.testing.assert_allclose(np_(scores), ref_sc, rtol=1e-5, atol=atol)
+    err = np.abs(np_(scores).astype(np.float64) - ref_sc)
+    if cfg.dtype == "bf16":
+        # the bound from each score's measured accumulator range, no assumed
+        # magnitude; the measured error must lie inside it everywhere
+        bound = tc_router_bound(np_(inp["x"]), np_(inp["w_router"]), fn == oracle.SIGMOID)
+        ratio = float((err / bound).max())
+        print(f"{name}: router max |err| {err.max():.3e}, max bound {bound.max():.3e}, "
+              f"max err/bound {ratio:.3f}")
+        assert ratio <= 1.0
+        atol = float(bound.max())
+    else:
+        atol = 2e-5
+        assert (err <= atol + 1e-5 * np.abs(ref_sc)).all()
     bias = np_(inp["bias"])
     ref_idx = oracle.select(ref_sc, cfg.k, bias=bias, n_group=cfg.n_group, topk_group=cfg.topk_group)
     got = np_(idx)
     differ = (got != ref_idx).any(1)
     amb = near_tie_tokens(ref_sc, bias, cfg.k, cfg.n_group, cfg.topk_group, rel=1e-5,
                           abs_margin=atol)
+    print(f"{name}: {int(differ.sum())} of {T} tokens chose differently from the oracle's own "
+          f"scores ({int(amb.sum())} near ties)")
     assert not (differ & ~amb).any(), f"{int((differ & ~amb).sum())} tokens differ without a near tie"
     assert differ.sum() <= max(2, T // 500)
 
@@ -101,8 +114,8 @@ def test_route_full_router(oracle, name):
                                       (1000, 1024, 130, "softmax"), (257, 7168, 256, "sigmoid")])
 def test_router_tensor_core_split_weight(oracle, T, d, E, fn):
     """bf16 activations: the tensor-core router with the fp32 weight split into
-    three bf16 terms matches the oracle's router to fp32 rounding (tails in
-    tokens, experts and K included)."""
+    three bf16 terms matches the oracle's router within the rounding bound of
+    its fp32 accumulation (tails in tokens, experts and K included)."""
     g = torch.Generator(device="cuda")
     g.manual_seed(T + d + E)
     x = torch.randn((T, d), generator=g, device="cuda").to(torch.bfloat16)
@@ -114,7 +127,9 @@ def test_router_tensor_core_split_weight(oracle, T, d, E, fn):
     torch.cuda.synchronize()
     ofn = oracle.SIGMOID if fn == "sigmoid" else oracle.SOFTMAX
     ref = oracle.router_scores(np_(x), np_(wr), ofn)
-    np.testing.assert_allclose(np_(scores), ref, rtol=1e-6, atol=tc_router_atol(d))
+    err = np.abs(np_(scores).astype(np.float64) - ref)
+    bound = tc_router_bound(np_(x), np_(wr), fn == "sigmoid")
+    assert (err <= bound).all(), f"max err/bound {(err / bound).max():.3f}"
 
 
 def test_split_router_weight_terms_sum_exactly():
