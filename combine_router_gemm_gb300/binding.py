@@ -50,13 +50,15 @@ class LayerArgs(ctypes.Structure):
                 ("route", RouteCfg), ("scores_out", ctypes.c_void_p),
                 ("topk_idx_out", ctypes.c_void_p), ("topk_w_out", ctypes.c_void_p),
                 ("offsets_out", ctypes.c_void_p), ("stage_events", ctypes.c_void_p),
-                ("flags", ctypes.c_int32), ("w_router_split", ctypes.c_void_p)]
+                ("flags", ctypes.c_int32), ("w_router_split", ctypes.c_void_p),
+                ("sync_events", ctypes.c_void_p)]
 
 LAYER_FUSED_COMBINE = 1
 LAYER_PACKED_WEIGHTS = 2
 LAYER_SHARED_AFTER_ROUTER = 4
 
 LAYER_EVENTS = 7
+LAYER_SYNC_EVENTS = 2
 
 
 _lib = None
@@ -255,10 +257,13 @@ def moe_combine(y_perm, slot_to_row, topk_w, shared, out, stream=None):
 
 def layer_args(x, w_router, bias, w13, w2, w13_sh, w2_sh, cfg: RouteCfg, scores_out=None,
                topk_idx_out=None, topk_w_out=None, offsets_out=None,
-               stage_events=None, flags: int = 0, w_router_split=None) -> LayerArgs:
+               stage_events=None, flags: int = 0, w_router_split=None,
+               sync_events=None) -> LayerArgs:
     """``stage_events``: None or a list of LAYER_EVENTS torch.cuda.Event (kept
     alive by the caller), recorded by the library at the stage boundaries.
-    ``w_router_split``: the router weight from moe_split_router_weight, or None."""
+    ``w_router_split``: the router weight from moe_split_router_weight, or None.
+    ``sync_events``: None or a list of LAYER_SYNC_EVENTS torch.cuda.Event (kept
+    alive by the caller) that fork and join the second stream."""
     T, d = x.shape
     I = w2.shape[2]
     I_sh = w2_sh.shape[1] if w2_sh is not None else 0
@@ -270,25 +275,26 @@ def layer_args(x, w_router, bias, w13, w2, w13_sh, w2_sh, cfg: RouteCfg, scores_
                      _ptr(topk_idx_out, torch.int32, "topk_idx_out"),
                      _ptr(topk_w_out, torch.float32, "topk_w_out"),
                      _ptr(offsets_out, torch.int32, "offsets_out"), _events(stage_events), flags,
-                     _ptr(w_router_split, torch.bfloat16, "w_router_split"))
+                     _ptr(w_router_split, torch.bfloat16, "w_router_split"),
+                     _events(sync_events, LAYER_SYNC_EVENTS))
 
 
 _event_arrays = {}
 
 
-def _events(evs):
+def _events(evs, n=LAYER_EVENTS):
     """Host array of cudaEvent_t handles for torch events (cached per list)."""
     if evs is None:
         return None
-    if len(evs) != LAYER_EVENTS:
-        raise ValueError(f"need {LAYER_EVENTS} events")
+    if len(evs) != n:
+        raise ValueError(f"need {n} events")
     key = tuple(id(e) for e in evs)
     arr = _event_arrays.get(key)
     if arr is None:
         for e in evs:  # torch creates the CUDA event lazily on first record
             if e.cuda_event == 0:
                 e.record()
-        arr = (ctypes.c_void_p * LAYER_EVENTS)(*[e.cuda_event for e in evs])
+        arr = (ctypes.c_void_p * n)(*[e.cuda_event for e in evs])
         _event_arrays[key] = (arr, evs)
     else:
         arr = arr[0]
@@ -409,12 +415,16 @@ class MoELayer:
         self.ws_bytes = moe_layer_workspace_size(sizes)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.stream2 = torch.cuda.Stream(device=dev) if overlap and w13_sh is not None else None
+        # the two events that fork and join the second stream, made once
+        self.sync_events = ([torch.cuda.Event() for _ in range(LAYER_SYNC_EVENTS)]
+                            if self.stream2 is not None else None)
 
     def _args(self, x, **outs):
         w = self.w
         return layer_args(x, w["w_router"], w["bias"], w["w13"], w["w2"], w["w13_sh"],
                           w["w2_sh"], self.cfg, flags=self.flags | self._extra_flags,
-                          w_router_split=self.w_router_split, **outs)
+                          w_router_split=self.w_router_split, sync_events=self.sync_events,
+                          **outs)
 
     def forward(self, x, out=None, stream=None, **outs):
         """out [T,d] fp32 for x [T,d] (device tensors), enqueued on `stream`

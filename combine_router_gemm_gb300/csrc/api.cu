@@ -10,7 +10,7 @@
 
 namespace moe_f32 {
 int grouped_ffn_f32(const float* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
-                    const float* w13, const float* w2, float* y, float* h, const uint32_t* err,
+                    const float* w13, const float* w2, float* y, float* h, uint32_t* err,
                     cudaStream_t s);
 }
 
@@ -328,7 +328,8 @@ int moe_grouped_ffn(const void* x_perm, const int32_t* offsets, int E, int rows,
 int moe_combine(const float* y_perm, const int32_t* slot_to_row, const float* topk_w,
                 const float* shared, int T, int k, int d, float* out, void* stream) {
     if (T < 0 || k < 1 || d < 4 || d % 4) return MOE_ERR_INVALID_ARG;
-    if (k > 32) return MOE_ERR_UNSUPPORTED;
+    // the kernel indexes rows of y_perm with int: T*k must stay well inside it
+    if (k > 32 || (long long)T * k > INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
     if (!y_perm || !slot_to_row || !topk_w || !out) return MOE_ERR_INVALID_ARG;
     if (!moe_host::aligned16(y_perm) || !moe_host::aligned16(out) ||
         (shared && !moe_host::aligned16(shared)))
@@ -384,7 +385,14 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
                              /*in_gate_up=*/!two_streams, /*in_down=*/true};
     cudaEvent_t ev_start = nullptr, ev_shared = nullptr;
     const bool overlap = sh && two_streams;
-    if (overlap &&
+    // fork/join events: the caller's, else two made (and destroyed) here
+    const bool own_events = overlap && !a->sync_events;
+    if (overlap && a->sync_events) {
+        ev_start = static_cast<cudaEvent_t>(a->sync_events[0]);
+        ev_shared = static_cast<cudaEvent_t>(a->sync_events[1]);
+        if (!ev_start || !ev_shared) return MOE_ERR_INVALID_ARG;
+    }
+    if (own_events &&
         (cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) != cudaSuccess ||
          cudaEventCreateWithFlags(&ev_shared, cudaEventDisableTiming) != cudaSuccess)) {
         if (ev_start) cudaEventDestroy(ev_start);
@@ -452,8 +460,10 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     if (rc == MOE_OK && !fused)
         rc = moe_launch::combine(w.yp, w.s2r, w.w, w.ysh, T, k, d, out, w.err, s0);
     mark(6);
-    if (ev_start) cudaEventDestroy(ev_start);
-    if (ev_shared) cudaEventDestroy(ev_shared);
+    if (own_events) {
+        cudaEventDestroy(ev_start);
+        cudaEventDestroy(ev_shared);
+    }
     return rc;
 }
 

@@ -20,7 +20,7 @@ __global__ void __launch_bounds__(256) ffn_f32_kernel(const float* __restrict__ 
                                                       const float* __restrict__ B,
                                                       size_t b_expert_stride, int N_out,
                                                       int up_off, float* __restrict__ Cout,
-                                                      const uint32_t* err) {
+                                                      uint32_t* err) {
     __shared__ float As[FT][FT + 1];
     __shared__ float Bg[FT][FT + 1];
     __shared__ float Bu[FT][FT + 1];
@@ -33,7 +33,11 @@ __global__ void __launch_bounds__(256) ffn_f32_kernel(const float* __restrict__ 
             for (int i = 0; i < E; ++i) {
                 const int a = offsets ? offsets[i] : 0;
                 const int b = offsets ? offsets[i + 1] : rows;
-                if (a < 0 || b < a || b > rows) break;
+                if (a < 0 || b < a || b > rows) {
+                    // inconsistent offsets: report them; this block computes nothing
+                    moe::raise_error(err, moe::ERR_BAD_OFFSETS);
+                    break;
+                }
                 const int nt = (b - a + FT - 1) / FT;
                 if (tile < nt) {
                     e = i;
@@ -96,7 +100,7 @@ __global__ void __launch_bounds__(256) ffn_f32_kernel(const float* __restrict__ 
 namespace moe_f32 {
 
 int grouped_ffn_f32(const float* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
-                    const float* w13, const float* w2, float* y, float* h, const uint32_t* err,
+                    const float* w13, const float* w2, float* y, float* h, uint32_t* err,
                     cudaStream_t s) {
     const int mtiles = moe::ceil_div(rows, FT) + E;
     dim3 g1(mtiles, moe::ceil_div(I, FT));

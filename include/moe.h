@@ -73,15 +73,20 @@ typedef struct {
     float routed_scale;
 } moe_route_cfg;
 
-/* Human-readable name of a status code (static string, never NULL). */
+/* Source: the pages have no counterpart (library support call).
+ * Human-readable name of a status code (static string, never NULL). */
 const char* moe_status_string(int status);
 
-/* ABI version (major * 100 + minor). */
+/* Source: the pages have no counterpart (library support call).
+ * ABI version (major * 100 + minor). */
 int moe_version(void);
 
 /* ---------------------------------------------------------------- routing */
 
-/* Top-k selection and gates from a given fp32 score tensor.
+/* Source: the pages define no interface; this is the routing that decides
+ * the dispatch of Table 4, row "MoE Dispatch/Combine", read as DeepSeek-V3 /
+ * Mixtral top-k routing.
+ * Top-k selection and gates from a given fp32 score tensor.
  *   scores   [T,E] fp32: logits (softmax) or sigmoid outputs (sigmoid)
  *   bias     [E] fp32 or NULL: added to the scores for SELECTION only
  *            (DeepSeek-V3 style); must be NULL for softmax
@@ -96,18 +101,24 @@ int moe_route_from_scores(const float* scores, const float* bias, int T,
                           const moe_route_cfg* cfg, int32_t* topk_idx, float* topk_w,
                           void* stream);
 
-/* Workspace bytes moe_route needs (T tokens, E experts, hidden size d). */
+/* Source: the pages have no counterpart (sizing query).
+ * Workspace bytes moe_route needs (T tokens, E experts, hidden size d). */
 size_t moe_route_workspace_size(int T, int E, int d, int dtype);
 
-/* Router GEMM then moe_route_from_scores.
+/* Source: the pages define no interface; the router of the DeepSeek-V3 MoE
+ * layer named in the abstract and Table 4, row "MoE Dispatch/Combine".
+ * Router GEMM then moe_route_from_scores.
  *   x        [T,d] bf16 or fp32 (dtype)
  *   w_router [E,d] fp32
  *   scores   [T,E] fp32 out (logits, or sigmoid(logits)); fp32 accumulate
  * bf16 x: tcgen05 tensor cores, with w_router split into three bf16 terms
  * (hi + mid + lo, each the bf16 rounding of what the previous leave) so that
- * every product is exact and sums are fp32 -- the result matches an fp32
- * GEMM to fp32 rounding; the K range may be cut into parts whose partial sums
- * are added (in order) before the sigmoid.  fp32 x: CUDA cores in fp32.
+ * every product is exact and only the fp32 accumulation rounds: each logit
+ * is within (ceil(d/16) + 6) * 2^-23 * R of the exact dot product, R the
+ * range of its running sum over steps of 16 products (a sigmoid score within
+ * a quarter of that plus 2^-21); the K range may be cut into parts whose
+ * partial sums are added (in order) before the sigmoid.  fp32 x: CUDA cores
+ * in fp32.
  * ws: moe_route_workspace_size bytes (error word, split weight, partials). */
 int moe_route(const void* x, int dtype, const float* w_router, const float* bias, int T, int d,
               const moe_route_cfg* cfg, float* scores, int32_t* topk_idx, float* topk_w, void* ws,
@@ -115,10 +126,14 @@ int moe_route(const void* x, int dtype, const float* w_router, const float* bias
 
 /* --------------------------------------------------------------- dispatch */
 
-/* Workspace bytes moe_dispatch needs for T tokens, k slots, E experts. */
+/* Source: the pages have no counterpart (sizing query).
+ * Workspace bytes moe_dispatch needs for T tokens, k slots, E experts. */
 size_t moe_dispatch_workspace_size(int T, int k, int E);
 
-/* Stable counting sort of the S = T*k slots (s = t*k + j) by expert, then the
+/* Source: the pages define no interface; the dispatch half of Table 4, row
+ * "MoE Dispatch/Combine", on one GPU a stable sort of the slots by expert
+ * and a row gather into unpadded expert segments.
+ * Stable counting sort of the S = T*k slots (s = t*k + j) by expert, then the
  * row gather.  Outputs (all int32 unless noted):
  *   counts[E]        slots routed to each expert
  *   offsets[E+1]     exclusive prefix of counts, offsets[E] = S
@@ -136,10 +151,14 @@ int moe_dispatch(const int32_t* topk_idx, const void* x, int dtype, int T, int d
 
 /* ------------------------------------------------------------ expert FFN */
 
-/* Workspace bytes moe_grouped_ffn needs for `rows` permuted rows. */
+/* Source: the pages have no counterpart (sizing query).
+ * Workspace bytes moe_grouped_ffn needs for `rows` permuted rows. */
 size_t moe_grouped_ffn_workspace_size(int rows, int d, int I, int dtype);
 
-/* Per-expert SwiGLU FFN over permuted rows, as two grouped GEMMs:
+/* Source: the pages define no interface; the local expert compute between
+ * dispatch and combine (Table 4, row "MoE Dispatch/Combine", whose padding
+ * overhead on imbalanced loads the exact segments here avoid).
+ * Per-expert SwiGLU FFN over permuted rows, as two grouped GEMMs:
  *   rows [offsets[e], offsets[e+1]) belong to expert e (offsets on device,
  *   E+1 int32, non-decreasing, offsets[E] <= rows);
  *   H[r]  = silu(x_perm[r] W1_e^T) * (x_perm[r] W3_e^T)   (bf16 for bf16)
@@ -156,7 +175,9 @@ int moe_grouped_ffn(const void* x_perm, const int32_t* offsets, int E, int rows,
 
 /* ---------------------------------------------------------------- combine */
 
-/* out[t,:] = sum_{j<k} topk_w[t,j] * y_perm[slot_to_row[t*k+j], :]  (+ shared[t,:])
+/* Source: the pages define no interface; the combine half of Table 4, row
+ * "MoE Dispatch/Combine": each token's expert results weighted and summed.
+ * out[t,:] = sum_{j<k} topk_w[t,j] * y_perm[slot_to_row[t*k+j], :]  (+ shared[t,:])
  * summed in slot order in fp32.  y_perm [S,d] fp32, shared [T,d] fp32 or NULL,
  * out [T,d] fp32 (must not alias the inputs). */
 int moe_combine(const float* y_perm, const int32_t* slot_to_row, const float* topk_w,
@@ -196,7 +217,17 @@ typedef struct {
     /* bf16 only, optional: w_router already split by moe_split_router_weight
      * ([3,E,d] bf16), so that the call skips that step; NULL: split per call */
     const void* w_router_split;
+    /* optional: MOE_LAYER_SYNC_EVENTS cudaEvent_t handles (host array,
+     * caller-created, timing disabled is best) with which the call forks
+     * stream2 from `stream` and joins it back.  NULL: the call creates and
+     * destroys two events itself, a host-side cost on every call.  A caller
+     * that reuses them must not record them elsewhere while a call that
+     * uses them is being enqueued. */
+    void* const* sync_events;
 } moe_layer_args;
+
+/* Number of events in moe_layer_args.sync_events. */
+#define MOE_LAYER_SYNC_EVENTS 2
 
 /* moe_layer_args.flags: add the down projection's results straight into `out`
  * (16-byte fp32 vector reductions in the grouped GEMM's epilogue) instead of
@@ -219,13 +250,17 @@ typedef struct {
  * the same either way. */
 #define MOE_LAYER_SHARED_AFTER_ROUTER 4
 
-/* Workspace bytes moe_layer needs (0 for invalid sizes or configuration).
+/* Source: the pages have no counterpart (sizing query).
+ * Workspace bytes moe_layer needs (0 for invalid sizes or configuration).
  * Only the sizes, dtype, routing configuration, I_sh (> 0: shared expert
  * present) and which optional outputs are non-NULL matter here; the input
  * pointers may still be NULL. */
 size_t moe_layer_workspace_size(const moe_layer_args* a);
 
-/* out [T,d] fp32 = the layer: route, dispatch, grouped FFN, shared expert,
+/* Source: the pages define no interface; the whole DeepSeek-V3 MoE layer of
+ * the abstract and Table 4, row "MoE Dispatch/Combine" (with its two-stream
+ * overlap, on one GPU: the shared expert on stream2).
+ * out [T,d] fp32 = the layer: route, dispatch, grouped FFN, shared expert,
  * combine.  `stream2` (may be NULL) is a second stream of the same device.
  * Given stream2, the shared expert's two GEMMs run there, launched with the
  * router GEMM and concurrent with it, top-k and dispatch (with
@@ -239,7 +274,8 @@ size_t moe_layer_workspace_size(const moe_layer_args* a);
 int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, void* stream,
               void* stream2);
 
-/* Expert weights into the tile-major layouts of MOE_LAYER_PACKED_WEIGHTS, a
+/* Source: the pages have no counterpart (a one-time weight preparation).
+ * Expert weights into the tile-major layouts of MOE_LAYER_PACKED_WEIGHTS, a
  * one-time preparation of a layer's weights.  Each 128-row x 64-column tile
  * (16 KB of bf16) is stored contiguously, so that the grouped GEMMs read it
  * from HBM in one piece rather than as 128 pieces one matrix row apart.
@@ -255,7 +291,8 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
 int moe_pack_expert_weights(const void* w13, const void* w2, int E, int d, int I,
                             void* w13_packed, void* w2_packed, void* stream);
 
-/* The fp32 router weight [E,d] as the three bf16 terms the tensor-core router
+/* Source: the pages have no counterpart (a one-time weight preparation).
+ * The fp32 router weight [E,d] as the three bf16 terms the tensor-core router
  * multiplies (out [3,E,d] bf16: hi, mid, lo, each term the bf16 rounding of
  * what the previous ones leave; w = hi + mid + lo exactly for |w| >= 2^-110,
  * to within 2^-134 below, where bf16's finest spacing ends), for
@@ -278,9 +315,11 @@ int moe_split_router_weight(const float* w_router, int E, int d, void* out, void
  * which every GPU that loads the library holds until the process exits.
  *   - T*k above MOE_DISPATCH_NOALLOC_MAX_SLOTS or E above 1024 is refused
  *     with MOE_ERR_UNSUPPORTED; nothing is enqueued.
- *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current) and caches it; make that first
- *     call before any stream capture.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it with the identity of the current
+ *     CUDA context; a call in a different context (after cudaDeviceReset,
+ *     say) looks it up again.  Make the first call on a device, and the
+ *     first after such a reset, before any stream capture.
  *   - All calls share the one array, which keeps the last call's contents
  *     (each call clears what must start at zero).  Calls that may overlap on
  *     the GPU -- on different streams without ordering between them -- race
@@ -294,13 +333,15 @@ int moe_dispatch_noalloc(const int32_t* topk_idx, const void* x, int dtype, int 
                          int32_t* row_to_token, void* x_perm, uint32_t* device_error,
                          void* stream);
 
-/* Synchronises `stream`, reads and clears the error word of `ws` (a workspace
+/* Source: the pages have no counterpart (failure detection support).
+ * Synchronises `stream`, reads and clears the error word of `ws` (a workspace
  * previously passed to moe_dispatch / moe_grouped_ffn / moe_layer).  Returns
  * MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_INPUT or MOE_ERR_CUDA.  `detail`
  * (host pointer, may be NULL) receives the raw error word. */
 int moe_check_error(void* ws, void* stream, uint32_t* detail);
 
-/* Self-test of the bounded device waits (failure detection without a fault).
+/* Source: the pages have no counterpart (failure detection support).
+ * Self-test of the bounded device waits (failure detection without a fault).
  * Launches one tiny kernel that waits on something nothing will ever signal:
  * which = 0: an mbarrier, as in the grouped-GEMM pipeline; which = 1: a
  * predecessor's look-back flag, as in the dispatch scan.  The wait gives up

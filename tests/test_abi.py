@@ -34,6 +34,29 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_struct_layouts_match_the_header(tmp_path):
+    """The ctypes structures have the C structures' field offsets and sizes
+    (a small C program built against include/moe.h prints them)."""
+    fields = {"moe_route_cfg": B.RouteCfg, "moe_layer_args": B.LayerArgs}
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "moe.h"', 'int main(void) {']
+    for cname, py in fields.items():
+        lines.append(f'printf("{cname} sizeof %zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    import subprocess
+    subprocess.run(["gcc", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    got = {tuple(ln.split()[:2]): int(ln.split()[2]) for ln in out.splitlines()}
+    for cname, py in fields.items():
+        assert got[(cname, "sizeof")] == ctypes.sizeof(py), cname
+        for f, _ in py._fields_:
+            assert got[(cname, f)] == getattr(py, f).offset, (cname, f)
+
+
 def test_status_strings(lib):
     assert B.status_string(B.OK) == "ok"
     for s in range(1, 7):

@@ -95,14 +95,17 @@ def test_grouped_ffn_f32(oracle, E, d, I, counts):
     assert rel_fro(np_(y)[:n], ref) <= F32_REL_FRO
 
 
-def test_grouped_ffn_bad_offsets_flagged():
-    # Non-monotone device offsets: the kernels do no work and flag the input.
-    x, offsets, w13, w2 = make_case(2, 128, 128, [10, 10], torch.bfloat16, seed=1)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_grouped_ffn_bad_offsets_flagged(dtype):
+    # Non-monotone device offsets: the kernels do no work and flag the input
+    # (tensor-core path and fp32 CUDA-core path alike).
+    x, offsets, w13, w2 = make_case(2, 128, 128, [10, 10], dtype, seed=1)
     offsets[1] = 15
     offsets[2] = 12
     rows, d = x.shape
     y = cuda_f32((rows, d))
-    ws = torch.empty(B.moe_grouped_ffn_workspace_size(rows, d, 128, B.BF16), dtype=torch.uint8,
+    code = B.BF16 if dtype == torch.bfloat16 else B.F32
+    ws = torch.empty(B.moe_grouped_ffn_workspace_size(rows, d, 128, code), dtype=torch.uint8,
                      device="cuda")
     B.moe_grouped_ffn(x, offsets, w13, w2, y, ws)
     rc, detail = B.moe_check_error(ws)
