@@ -56,9 +56,8 @@ NOMINAL_HBM_GBS = 7900.0
 NOMINAL_BF16_TFLOPS = 2250.0
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the routed
-# gate/up GEMM per launch, from ncu captures of this kernel source
-# (profiles/grouped_gemm_tc_dsv3_prefill_dram.md, ..._e32.md).  Reported as
-# null once the kernel source no longer matches the captured one.
+# gate/up GEMM per launch, from ncu captures of this kernel source.  Reported
+# as null once the kernel source no longer matches the captured one.
 TRAFFIC = {"source_sha256": "2fa131f32e04477848d0b763103c9eece876dd7f1e4f0bdc14a7a607a44d91fa",
            # routed gate/up launch on tile-major weights (the shared expert
            # runs on the second stream): dsv3_prefill from a one-pass capture
@@ -367,105 +366,17 @@ def kernel_source_sha():
     return hashlib.sha256(open(p, "rb").read()).hexdigest()
 
 
-def run_ours(args, cfg):
-    import torch
-    import torch.distributed as dist
-
-    rank, local_rank, world = env_rank()
-    torch.cuda.set_device(local_rank)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-
-    from combine_router_gemm_gb300 import binding as B
-    from combine_router_gemm_gb300 import build as build_mod
-    from combine_router_gemm_gb300 import inputs
-    build_mod.build()
-
-    pk = peaks()
-    inp = inputs.make_inputs(cfg, seed=0, device="cuda")
-    layer = B.MoELayer(inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"],
-                       inp["w2_sh"], B.cfg_from(cfg), cfg.T, overlap=not args.no_overlap,
-                       fused_combine=args.fused_combine, pack_weights=not args.row_major_weights)
-    x = inp["x"]
-    out = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device="cuda")
-    offs = torch.empty(cfg.E + 1, dtype=torch.int32, device="cuda")
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    warm = max(3, args.warmup)
-    for _ in range(warm):
-        layer.forward(x, out=out, offsets_out=offs)
-    rc, detail = B.moe_check_error(layer.ws)
-    if rc != B.OK:
-        raise RuntimeError(f"device error word {detail:#x} during warm-up")
-
-    K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(B.LAYER_EVENTS)] for _ in range(K)]
-    # the layer also recorded once into a CUDA graph (both streams) and
-    # replayed, as a second timing of the same steps
-    graph = None
-    if not args.no_graph:
-        graph, gout = layer.capture(x, offsets_out=offs)
-        for _ in range(warm):
-            graph.replay()
-    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)]
-    with ClockSampler(local_rank) as clk:
-        # pass 1 (the reported value): stream-launched calls with stage events
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter()
-        for s in range(K):
-            flush.zero_()
-            layer.forward(x, out=out, offsets_out=offs, stage_events=evs[s])
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
-        if world > 1:
-            dist.barrier()
-        # pass 2: graph replays of the same call (inputs resident, L2 flushed
-        # between steps)
-        if graph is not None:
-            torch.cuda.synchronize()
-            for s in range(K):
-                flush.zero_()
-                gev[s][0].record()
-                graph.replay()
-                gev[s][1].record()
-            torch.cuda.synchronize()
-            if world > 1:
-                dist.barrier()
-    rc, detail = B.moe_check_error(layer.ws)
-    if rc != B.OK:
-        raise RuntimeError(f"device error word {detail:#x} during the timed steps")
-
-    step_ms = [e[0].elapsed_time(e[-1]) for e in evs]
-    stage_ms = [statistics.fmean(e[i].elapsed_time(e[i + 1]) for e in evs)
-                for i in range(B.LAYER_EVENTS - 1)]
-    total_s = max_over_ranks(sum(step_ms) / 1e3)
-    value = whole_job_value(cfg.T, K, world, total_s)
-    graph_replay = None
-    if graph is not None:
-        g_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in gev) / 1e3)
-        graph_replay = {"value": whole_job_value(cfg.T, K, world, g_s), "unit": UNIT,
-                        "ms_per_step": 1e3 * g_s / K}
-        del graph, gout
-
-    # ---- algorithmic work per stage (bytes / flops per launch)
+def stage_metrics(cfg, stage_ms, offs, merged, merged_gu, pk):
+    """Per-stage algorithmic bytes and flops, rates and roofline fractions,
+    and the roofline object of the dominant kernel (the routed gate/up)."""
     o = offs.cpu().numpy()
     active = int((o[1:] - o[:-1] > 0).sum())
-    S, d, I, T, E = cfg.S, cfg.d, cfg.I, cfg.T, cfg.E
+    S, d, I, T = cfg.S, cfg.d, cfg.I, cfg.T
     es = 2 if cfg.dtype == "bf16" else 4
     gu_bytes = active * 2 * I * d * es + S * d * es + S * I * es
     gu_flops = 2.0 * S * d * 2 * I
     dn_bytes = active * d * I * es + S * I * es + S * d * 4
     dn_flops = 2.0 * S * I * d
-    # bf16, I_sh == I: with a second stream the shared expert runs there in
-    # launches of its own (with the fused combine, only its gate/up; its down
-    # tiles ride in the routed down launch); without one, both halves ride
-    # in the routed launches
-    two_streams = layer.stream2 is not None
-    merged = (bool(cfg.shared_I) and cfg.dtype == "bf16" and cfg.shared_I == cfg.I
-              and (not two_streams or args.fused_combine))
-    merged_gu = merged and not two_streams
     Is = cfg.shared_I
     if merged_gu:
         gu_bytes += 2 * Is * d * es + T * d * es + T * Is * es
@@ -488,10 +399,6 @@ def run_ours(args, cfg):
     stages["dispatch"].update(GBps=round(bw(perm_bytes, stage_ms[2]), 1),
                               frac_hbm=round(bw(perm_bytes, stage_ms[2]) / pk["hbm_gbs"], 4),
                               note="count + permute, beside the shared expert's GEMMs")
-    # the dispatch (count + permute) alone, on this step's routing
-    d_ms = dispatch_alone_ms(cfg, x, layer, flush, steps=min(K, 20))
-    stages["dispatch_alone"] = {"ms": round(d_ms, 4), "GBps": round(bw(perm_bytes, d_ms), 1),
-                                "frac_hbm": round(bw(perm_bytes, d_ms) / pk["hbm_gbs"], 4)}
     for key, b, f, ms in (("gate_up_gemm", gu_bytes, gu_flops, stage_ms[3]),
                           ("down_gemm", dn_bytes, dn_flops, stage_ms[4])):
         stages[key].update(GBps=round(bw(b, ms), 1), TFLOPs=round(tf(f, ms), 1),
@@ -519,6 +426,161 @@ def run_ours(args, cfg):
     # (HBM3e 7.9 TB/s, dense bf16 2.25 PFLOP/s)
     nominal = NOMINAL_HBM_GBS if roof["bound"] == "hbm" else NOMINAL_BF16_TFLOPS
     roof.update(nominal_peak=nominal, frac_of_nominal=round(roof["achieved"] / nominal, 4))
+    return stages, roof, active, perm_bytes
+
+
+def measure_layer(cfg, args, layer, x, flush, pk, K, warm, clk_dev, world, graph_too):
+    """Warm-up, then K stream-launched layer calls (L2 flushed before each,
+    stage events recorded, clocks sampled), optionally K graph replays of the
+    same call in the same clock-sampled region.  Returns the measured figures."""
+    import torch
+    import torch.distributed as dist
+    from combine_router_gemm_gb300 import binding as B
+
+    out = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device="cuda")
+    offs = torch.empty(cfg.E + 1, dtype=torch.int32, device="cuda")
+    for _ in range(warm):
+        layer.forward(x, out=out, offsets_out=offs)
+    rc, detail = B.moe_check_error(layer.ws)
+    if rc != B.OK:
+        raise RuntimeError(f"device error word {detail:#x} during warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(B.LAYER_EVENTS)] for _ in range(K)]
+    graph = None
+    if graph_too:
+        graph, gout = layer.capture(x, offsets_out=offs)
+        for _ in range(warm):
+            graph.replay()
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    with ClockSampler(clk_dev) as clk:
+        # pass 1 (the reported value): stream-launched calls with stage events
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        for s in range(K):
+            flush.zero_()
+            layer.forward(x, out=out, offsets_out=offs, stage_events=evs[s])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        if world > 1:
+            dist.barrier()
+        # pass 2: graph replays of the same call (inputs resident, L2 flushed
+        # between steps)
+        if graph is not None:
+            torch.cuda.synchronize()
+            for s in range(K):
+                flush.zero_()
+                gev[s][0].record()
+                graph.replay()
+                gev[s][1].record()
+            torch.cuda.synchronize()
+            if world > 1:
+                dist.barrier()
+    rc, detail = B.moe_check_error(layer.ws)
+    if rc != B.OK:
+        raise RuntimeError(f"device error word {detail:#x} during the timed steps")
+    step_ms = [e[0].elapsed_time(e[-1]) for e in evs]
+    stage_ms = [statistics.fmean(e[i].elapsed_time(e[i + 1]) for e in evs)
+                for i in range(B.LAYER_EVENTS - 1)]
+    total_s = max_over_ranks(sum(step_ms) / 1e3)
+    res = {"value": whole_job_value(cfg.T, K, world, total_s), "ms_per_step": 1e3 * total_s / K,
+           "steps": K, "warmup": warm, "clocks": clk.summary(), "wall_s_timed": round(t_wall, 3)}
+    if graph is not None:
+        g_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in gev) / 1e3)
+        res["graph_replay"] = {"value": whole_job_value(cfg.T, K, world, g_s), "unit": UNIT,
+                               "ms_per_step": 1e3 * g_s / K}
+        del graph, gout
+    # bf16, I_sh == I: with a second stream the shared expert runs there in
+    # launches of its own (with the fused combine, only its gate/up; its down
+    # tiles ride in the routed down launch); without one, both halves ride
+    # in the routed launches
+    two_streams = layer.stream2 is not None
+    merged = (bool(cfg.shared_I) and cfg.dtype == "bf16" and cfg.shared_I == cfg.I
+              and (not two_streams or args.fused_combine))
+    stages, roof, active, perm_bytes = stage_metrics(cfg, stage_ms, offs, merged,
+                                                     merged and not two_streams, pk)
+    # the dispatch (count + permute) alone, on this step's routing
+    d_ms = dispatch_alone_ms(cfg, x, layer, flush, steps=min(K, 20))
+    gbs = perm_bytes / (d_ms * 1e-3) / 1e9
+    stages["dispatch_alone"] = {"ms": round(d_ms, 4), "GBps": round(gbs, 1),
+                                "frac_hbm": round(gbs / pk["hbm_gbs"], 4)}
+    res.update(stages=stages, roofline=roof, active_experts=active, two_streams=two_streams)
+    return res
+
+
+def make_layer(cfg, args, inp):
+    from combine_router_gemm_gb300 import binding as B
+    return B.MoELayer(inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"],
+                      inp["w2_sh"], B.cfg_from(cfg), cfg.T, overlap=not args.no_overlap,
+                      fused_combine=args.fused_combine, pack_weights=not args.row_major_weights)
+
+
+# the other workloads timed beside the headline one (N = 1), each with the
+# same protocol but fewer steps and without the host-side legs
+EXTRA_WORKLOADS = ("mixtral_bf16", "dsv3_decode", "dsv3_zipf")
+
+
+def extra_workloads(args, pk, flush, names):
+    """Each named workload built, timed and freed in turn."""
+    import gc
+
+    import torch
+    from combine_router_gemm_gb300 import inputs
+    res = {}
+    for name in names:
+        cfg = inputs.CONFIGS[name]
+        inp = inputs.make_inputs(cfg, seed=0, device="cuda")
+        layer = make_layer(cfg, args, inp)
+        x = inp["x"]
+        for k in ("w13", "w2", "w13_sh", "w2_sh"):  # the layer holds its own copies
+            if layer.packed:
+                inp[k] = None
+        m = measure_layer(cfg, args, layer, x, flush, pk, min(args.steps, 30), 3, 0, 1, False)
+        m["config"] = config_dict(cfg)
+        m["dtype"] = cfg.dtype
+        res[name] = m
+        del layer, inp, x
+        gc.collect()
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, cfg):
+    import gc
+
+    import torch
+    import torch.distributed as dist
+
+    rank, local_rank, world = env_rank()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    from combine_router_gemm_gb300 import binding as B
+    from combine_router_gemm_gb300 import build as build_mod
+    from combine_router_gemm_gb300 import inputs
+    build_mod.build()
+
+    pk = peaks()
+    inp = inputs.make_inputs(cfg, seed=0, device="cuda")
+    layer = make_layer(cfg, args, inp)
+    x = inp["x"]
+    host_legs = rank == 0 and world == 1 and not (args.no_cpu_baseline and args.no_comparators)
+    if layer.packed and not host_legs:
+        # the layer holds the packed copies; the row-major originals are only
+        # needed by the comparator and the CPU oracle legs
+        for k in ("w13", "w2", "w13_sh", "w2_sh"):
+            inp[k] = None
+        gc.collect()
+        torch.cuda.empty_cache()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    K = args.steps
+    warm = max(3, args.warmup)
+    m = measure_layer(cfg, args, layer, x, flush, pk, K, warm, local_rank, world,
+                      graph_too=not args.no_graph)
+    presplit = layer.w_router_split is not None
+    T, d = cfg.T, cfg.d
 
     # ---- end to end through the public API with host buffers: every step
     # copies its input from pinned host memory and its output back; copies of
@@ -544,7 +606,7 @@ def run_ours(args, cfg):
 
     comp = None
     if rank == 0 and world == 1 and not args.no_comparators:
-        layer.forward(x, out=out)
+        out = layer.forward(x)
         torch.cuda.synchronize()
         comp = comparators(cfg, inp, out, flush)
 
@@ -552,23 +614,32 @@ def run_ours(args, cfg):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg, inp)
 
+    extras = None
+    if world == 1 and not args.no_workloads:
+        names = [n for n in EXTRA_WORKLOADS if n != cfg.name]
+        del layer, inp, x
+        gc.collect()
+        torch.cuda.empty_cache()
+        extras = extra_workloads(args, pk, flush, names)
+
     if rank == 0:
-        launches = launches_per_step(cfg, two_streams, args.fused_combine,
-                                     layer.w_router_split is not None) * K
+        launches = launches_per_step(cfg, m["two_streams"], args.fused_combine, presplit) * K
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": warm, "ms_per_step": 1e3 * total_s / K, "higher_is_better": True,
+            "metric": METRIC, "value": m["value"], "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": warm, "ms_per_step": m["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
             "config": {**config_dict(cfg), "expert_weights": "tile-major, packed once at layer "
-                       "construction" if layer.packed else "row-major"},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clk.summary(), "stages": stages,
-            "active_experts": active, "wall_s_timed": round(t_wall, 3),
+                       "construction" if not args.row_major_weights else "row-major"},
+            "roofline": m["roofline"], "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": m["clocks"], "stages": m["stages"],
+            "active_experts": m["active_experts"], "wall_s_timed": m["wall_s_timed"],
         }
-        if graph_replay:
-            line["graph_replay"] = graph_replay
+        if "graph_replay" in m:
+            line["graph_replay"] = m["graph_replay"]
         if comp:
             line["comparators"] = comp
+        if extras:
+            line["workloads"] = extras
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -588,6 +659,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-comparators", action="store_true",
                     help="skip the PyTorch comparator (the eager layer)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip timing the other workloads beside the headline one (N = 1)")
     ap.add_argument("--no-overlap", action="store_true", help="shared expert on the main stream")
     ap.add_argument("--row-major-weights", action="store_true",
                     help="keep the expert weights row-major (no tile-major packing)")

@@ -82,6 +82,17 @@ CONFIGS = {
     # DeepSeek-V3 layer shapes with 32 experts and 512 tokens: the same ~128
     # tokens per expert as dsv3_prefill in 1/8 of the memory (profiling case)
     "dsv3_prefill_e32": MoEConfig("dsv3_prefill_e32", T=512, **{**_DSV3, "E": 32}),
+    # the Zipf-imbalanced layer with 32 experts (4 of them empty) and 2048
+    # tokens: experts of ~250 to ~2000 rows, tensor-bound grouped GEMMs as in
+    # dsv3_zipf, in about 4 GB (profiling case)
+    "dsv3_zipf_e32": MoEConfig("dsv3_zipf_e32", T=2048,
+                               **{**_DSV3, "E": 32, "bias": "zipf", "zipf_zero": 4}),
+    # DeepSeek-V3 prefill routing, dispatch and combine at full size (4096
+    # tokens, 256 experts, d = 7168) with narrow experts (I = 128): the
+    # router, top-k, dispatch and combine kernels see the prefill shapes in
+    # about 3.5 GB (profiling case)
+    "dsv3_prefill_i128": MoEConfig("dsv3_prefill_i128", T=4096,
+                                   **{**_DSV3, "I": 128, "shared_I": 128}),
 }
 
 
