@@ -833,6 +833,549 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------- two-SM variant
+//
+// The same grouped GEMM on CTA pairs (clusters of two CTAs, one per SM of a
+// TPC) with tcgen05.mma.cta_group::2: one MMA computes 256 output features x
+// N tokens, the leader CTA (rank 0) holding 128 of the features and token
+// rows [0, N/2) of the tile, the follower (rank 1) the other 128 features
+// and token rows [N/2, N).  Each CTA loads two weight tiles per stage (gate/up:
+// its W1 and W3 tiles; down: two 128-feature tiles) and its half of the token
+// tile: 48 KB per SM and stage for 256 x 256 x 64 multiply-adds per SM, where
+// the one-SM tile loads 64 KB for the same work.  The grouped GEMMs are fed
+// at a rate bounded by the bytes each SM keeps in flight (measured: the MMA
+// thread of the one-SM kernel waits 20-27% of the time for its stages), so a
+// quarter fewer bytes per MMA is what the pair buys.
+//
+// Roles per CTA as in the one-SM kernel.  The leader's producer claims units
+// and publishes each unit index into both CTAs' rings (the follower's
+// through distributed shared memory); both producers load into their own
+// shared memory, completing on the LEADER's full barrier (the follower's
+// copies use the cta_group::2 form that may signal the peer's barrier).  The
+// leader's single MMA thread issues the pair's MMAs; its commits arrive on
+// both CTAs' stage-empty and accumulator-full barriers (multicast).  Both
+// CTAs' epilogue warps drain their own tensor memory and release the
+// accumulator on the leader's barrier.  Tensor memory is allocated and freed
+// collectively by one warp of each CTA.  Every wait is bounded; both CTAs
+// meet at a cluster barrier before tensor memory is freed and they exit.
+
+constexpr int BN2 = 256;  // token tile of a CTA pair (each CTA: 128 rows)
+
+// routed launches with 256-token tiles on CTA pairs (two-SM MMAs)
+#ifndef MOE_PAIR_GU
+#define MOE_PAIR_GU 1
+#endif
+#ifndef MOE_PAIR_DN
+#define MOE_PAIR_DN 1
+#endif
+
+template <int MODE>
+struct Cfg2 {
+    static constexpr int BN = BN2;
+    static constexpr int NUM_A = 2;       // weight tiles per CTA and stage
+    static constexpr int HB = BN / 2;     // token rows per CTA
+    static constexpr int STAGE_BYTES = NUM_A * A_TILE_BYTES + HB * BK * 2;
+    static constexpr int STAGES = SMEM_BUDGET / STAGE_BYTES;
+    static constexpr int ASTRIDE = 256;   // TMEM columns between the two accumulators
+    static constexpr int ACC_COLS = NUM_A * ASTRIDE;
+    static constexpr int ACC_STAGES = TMEM_COLS / ACC_COLS;
+    // output features per unit: gate/up, 256 features of W1 and the same of
+    // W3; down, 512 features (MMA a: features [n0 + 256a, n0 + 256a + 256),
+    // rank r holding the 128 from n0 + 256a + 128r)
+    static constexpr int FEAT = MODE == 1 ? 4 * BM : 2 * BM;
+    // row distance between a CTA's two weight tiles (gate/up: p.a_step = I)
+    static constexpr int A_STEP_DN = 2 * BM;
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + sizeof(int) * 2 * (MAX_E + 1);
+    static_assert(STAGES >= 2 && ACC_COLS <= TMEM_COLS && ACC_STAGES >= 1, "tile does not fit");
+    static_assert(HB % B_BOX == 0, "half tile must be whole boxes");
+    static_assert(SMEM + 64 <= (size_t)SMEM_LIMIT, "shared memory over the per-CTA limit");
+    // barriers + tensor-memory slot + flags + ring must fit the 256-byte area
+    static_assert((2 * STAGES + 2 * ACC_STAGES + 1 + 2 * RING) * 8 + 4 * (5 + RING) <= 256,
+                  "barrier area");
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(local), "r"(rank));
+    return d;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+// arrive on an mbarrier of another CTA of the cluster (cluster-scope release)
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_remote_u32(uint32_t cluster_addr, int v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// bounded wait with cluster-scope acquire (for barriers that the other CTA
+// arrives on, with data it wrote before arriving)
+__device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag, uint32_t* err,
+                                               uint64_t limit_ns) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = moe::globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (moe::globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            moe::raise_error(err, moe::ERR_TIMEOUT_PIPE);
+            return false;
+        }
+    }
+}
+
+// TMA load into this CTA's shared memory completing on a barrier of the
+// CTA pair (the leader's), cta_group::2 form
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes."
+        "cta_group::2 [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// commit the leader's MMAs so far to the barrier at this offset in both CTAs
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    const uint16_t mask = 3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                            const __grid_constant__ BMaps tm_b,
+                            const __grid_constant__ CUtensorMap tm_a2,
+                            const __grid_constant__ BMaps tm_b2, const Params p) {
+    using C = Cfg2<MODE>;
+    constexpr int STAGES = C::STAGES, NUM_A = C::NUM_A, ACC = C::ACC_STAGES, BN = C::BN;
+    constexpr int ACC_COLS = C::ACC_COLS, ASTRIDE = C::ASTRIDE, HB = C::HB;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* tiles = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)STAGES * C::STAGE_BYTES);
+    uint64_t* full_bar = bars;                // [STAGES] leader: both CTAs' copies
+    uint64_t* empty_bar = bars + STAGES;      // [STAGES] each CTA: its stage is free
+    uint64_t* tfull_bar = bars + 2 * STAGES;  // [ACC] each CTA: accumulator ready
+    uint64_t* tempty_bar = tfull_bar + ACC;   // [ACC] leader: both CTAs drained it
+    uint64_t* drain_bar = tempty_bar + ACC;   // [1]
+    uint64_t* ufull_bar = drain_bar + 1;      // [RING] each CTA: unit index published
+    uint64_t* uempty_bar = ufull_bar + RING;  // [RING] leader: read by all consumers
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(uempty_bar + RING);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* total_units = reinterpret_cast<int*>(tmem_slot + 2);
+    volatile int* ring = reinterpret_cast<volatile int*>(tmem_slot + 5);  // [RING]
+    int* mpre = reinterpret_cast<int*>(smem + (size_t)STAGES * C::STAGE_BYTES + 256);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+    // ---- schedule (both CTAs compute the same tables) ----
+    const int E = p.E;
+    const int n_tiles = (p.N_out + C::FEAT - 1) / C::FEAT;
+    const int U2 = p.rows2 > 0 ? ((p.rows2 + BN - 1) / BN) * n_tiles : 0;
+    int* pre_c = mpre;
+    int* pre_s = mpre + (E + 1);
+    if (warp == 0) {
+        const int per = (E + 31) / 32;
+        const int lo = min(E, lane * per), hi = min(E, lo + per);
+        int sum_c = 0, sum_s = 0;
+        bool bad = false;
+        for (int e = lo; e < hi; ++e) {
+            const int a = p.offsets ? p.offsets[e] : 0;
+            const int b = p.offsets ? p.offsets[e + 1] : p.rows;
+            if (a < 0 || b < a || b > p.rows) bad = true;
+            const int mt = (b - a + BN - 1) / BN;
+            if (b - a >= MOE_COMPUTE_ROWS) sum_c += mt; else sum_s += mt;
+        }
+        int inc_c = sum_c, inc_s = sum_s;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int oc = __shfl_up_sync(0xffffffffu, inc_c, off);
+            const int os = __shfl_up_sync(0xffffffffu, inc_s, off);
+            if (lane >= off) {
+                inc_c += oc;
+                inc_s += os;
+            }
+        }
+        int run_c = inc_c - sum_c, run_s = inc_s - sum_s;
+        for (int e = lo; e < hi; ++e) {
+            pre_c[e] = run_c;
+            pre_s[e] = run_s;
+            const int a = p.offsets ? p.offsets[e] : 0;
+            const int b = p.offsets ? p.offsets[e + 1] : p.rows;
+            const int mt = (b - a + BN - 1) / BN;
+            if (b - a >= MOE_COMPUTE_ROWS) run_c += mt; else run_s += mt;
+        }
+        const bool any_bad = __any_sync(0xffffffffu, bad);
+        if (lane == 31) {
+            pre_c[E] = inc_c;
+            pre_s[E] = inc_s;
+            const bool fail = any_bad || moe::read_error(p.err);
+            total_units[0] = fail ? -1 : (inc_c + inc_s) * n_tiles + U2;
+            total_units[1] = inc_c * n_tiles + U2;
+            total_units[2] = inc_s * n_tiles;
+            if (any_bad && leader) moe::raise_error(p.err, moe::ERR_BAD_OFFSETS);
+        }
+    }
+    if (tid == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int a = 0; a < ACC; ++a) {
+            mbar_init(smem_u32(&tfull_bar[a]), 1);
+            mbar_init(smem_u32(&tempty_bar[a]), 2 * NUM_EPI_WARPS);
+        }
+        mbar_init(smem_u32(drain_bar), 1);
+        for (int r = 0; r < RING; ++r) {
+            mbar_init(smem_u32(&ufull_bar[r]), 1);
+            // leader: its MMA thread and epilogue warps, the follower's
+            // producer and epilogue warps
+            mbar_init(smem_u32(&uempty_bar[r]), 2 + 2 * NUM_EPI_WARPS);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tm_a);
+        for (int i = 0; i < 4; ++i) tma_prefetch_desc(&tm_b.m[i]);
+        if (p.rows2 > 0) {
+            tma_prefetch_desc(&tm_a2);
+            for (int i = 0; i < 4; ++i) tma_prefetch_desc(&tm_b2.m[i]);
+        }
+    }
+    if (warp == 1) {
+        // collective: one warp of each CTA of the pair
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int U = total_units[0];
+
+    __shared__ int s_dense_offs[2];
+    if (tid == 0) {
+        s_dense_offs[0] = 0;
+        s_dense_offs[1] = p.rows;
+    }
+    __syncthreads();
+    const int* offs = p.offsets ? p.offsets : s_dense_offs;
+    const int num_kb = (p.K + BK - 1) / BK;
+    const Sched sched{pre_c, pre_s, offs, E, n_tiles, total_units[0], total_units[1],
+                      total_units[2], U2, p.rows2};
+    // the leader's barriers as cluster addresses (for the follower's arrivals)
+    const uint32_t leader_full0 = peer_addr(smem_u32(&full_bar[0]), 0);
+    const uint32_t leader_tempty0 = peer_addr(smem_u32(&tempty_bar[0]), 0);
+    const uint32_t leader_uempty0 = peer_addr(smem_u32(&uempty_bar[0]), 0);
+
+    if (U > 0 && warp == 0) {
+        // ================= TMA producer (one thread per CTA) =================
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int slot = 0;
+            uint32_t uphase = 0;
+            long issued = 0;
+            const uint32_t f_ring0 = peer_addr(smem_u32((const void*)&ring[0]), 1);
+            const uint32_t f_ufull0 = peer_addr(smem_u32(&ufull_bar[0]), 1);
+            int u = pair;
+            while (true) {
+                if (leader) {
+                    // publish u (or the end, -1) to both CTAs
+                    if (!mbar_wait_cluster(smem_u32(&uempty_bar[slot]), uphase ^ 1, abort_flag,
+                                           p.err, moe::WAIT_LIMIT_NS))
+                        break;
+                    const int v = (u >= U || *abort_flag) ? -1 : u;
+                    ring[slot] = v;
+                    st_remote_u32(f_ring0 + 4 * slot, v);
+                    mbar_arrive(smem_u32(&ufull_bar[slot]));
+                    mbar_arrive_remote(f_ufull0 + 8 * slot);
+                    u = v;
+                } else {
+                    if (!mbar_wait_cluster(smem_u32(&ufull_bar[slot]), uphase, abort_flag, p.err,
+                                           moe::WAIT_LIMIT_NS))
+                        break;
+                    u = ring[slot];
+                    mbar_arrive_remote(leader_uempty0 + 8 * slot);
+                }
+                if (++slot == RING) { slot = 0; uphase ^= 1; }
+                if (u < 0) break;
+                const int next = leader ? npairs + (int)atomicAdd(p.work, 1u) : 0;
+                const Unit t = decode_unit<BN, C::FEAT>(u, sched);
+                const CUtensorMap* ma = t.second ? &tm_a2 : &tm_a;
+                const CUtensorMap* mb = t.second ? tm_b2.m : tm_b.m;
+                const int bn = (t.n_tok + 31) & ~31;  // MMA N: a multiple of 32
+                const int hb = bn / 2;                // token rows per CTA
+                const int nbox = (hb + B_BOX - 1) / B_BOX;
+                const uint32_t cta_bytes = NUM_A * A_TILE_BYTES + nbox * B_BOX_BYTES;
+                const int a_row = (t.second ? 0 : t.e * p.a_rows) + t.n0 + (int)rank * BM;
+                const int a_step = MODE == 1 ? C::A_STEP_DN : p.a_step;
+                const int m0 = t.m_start + (int)rank * hb;
+                bool ok = true;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag, p.err,
+                                   moe::WAIT_LIMIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = tiles + (size_t)stage * C::STAGE_BYTES;
+                    const uint32_t fb = smem_u32(&full_bar[stage]);
+                    const uint32_t fb_pair = leader_full0 + 8 * stage;
+                    if (leader) mbar_arrive_expect_tx(fb, 2 * cta_bytes);
+                    const int kx = kb * BK;
+#pragma unroll
+                    for (int a = 0; a < NUM_A; ++a) {
+                        const int row = a_row + a * a_step;
+                        const int x = p.a_layout != WEIGHTS_ROWS ? 0 : kx;
+                        const int y = p.a_layout != WEIGHTS_ROWS
+                                          ? packed_tile(row / BM, kb, num_kb, p.a_layout) * BM
+                                          : row;
+                        if (leader)
+                            tma_load_2d(smem_u32(st + a * A_TILE_BYTES), ma, fb, x, y);
+                        else
+                            tma_load_2d_pair(smem_u32(st + a * A_TILE_BYTES), ma, fb_pair, x, y);
+                    }
+                    uint8_t* bdst = st + NUM_A * A_TILE_BYTES;
+                    int row = 0;
+#pragma unroll
+                    for (int lv = 2; lv >= 0; --lv) {  // boxes of 128/64/32 rows
+                        const int h = B_BOX << lv;
+                        if (h <= HB && (nbox * B_BOX - row) >= h) {
+                            if (leader)
+                                tma_load_2d(smem_u32(bdst + row * BK * 2), mb + lv, fb, kx,
+                                            m0 + row);
+                            else
+                                tma_load_2d_pair(smem_u32(bdst + row * BK * 2), mb + lv, fb_pair,
+                                                 kx, m0 + row);
+                            row += h;
+                        }
+                    }
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                if (leader) u = next;
+            }
+            if (*abort_flag && leader) {
+                // let the copies of this stage ring land before the CTA exits
+                for (int i = 0; i < STAGES && issued > 0; ++i, --issued) {
+                    if (stage == 0) { stage = STAGES; phase ^= 1; }
+                    --stage;
+                    const uint64_t t0 = moe::globaltimer_ns();
+                    while (!mbar_try_wait(smem_u32(&full_bar[stage]), phase) &&
+                           moe::globaltimer_ns() - t0 < 10000000ull) {
+                    }
+                }
+            }
+        }
+    } else if (U > 0 && warp == 1) {
+        // ================= MMA issuer (one thread of the leader) =================
+        if (lane == 0 && leader) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool issued_any = false;
+            int slot = 0;
+            uint32_t uphase = 0;
+            while (!*abort_flag) {
+                if (!mbar_wait(smem_u32(&ufull_bar[slot]), uphase, abort_flag, p.err,
+                               moe::WAIT_LIMIT_NS))
+                    break;
+                const int u = ring[slot];
+                mbar_arrive(smem_u32(&uempty_bar[slot]));
+                if (++slot == RING) { slot = 0; uphase ^= 1; }
+                if (u < 0) break;
+                const Unit t = decode_unit<BN, C::FEAT>(u, sched);
+                const int bn = (t.n_tok + 31) & ~31;
+                // M = 256 over the pair (bits 24-28: M / 16), N = bn
+                const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                       ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+                if (!mbar_wait_cluster(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, abort_flag, p.err,
+                                       moe::WAIT_LIMIT_NS))
+                    break;
+                tc_fence_after();
+                const uint32_t d0 = tmem_base + (uint32_t)(acc * ACC_COLS);
+                bool ok = true;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&full_bar[stage]), phase, abort_flag, p.err,
+                                   moe::WAIT_LIMIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = smem_u32(tiles + (size_t)stage * C::STAGE_BYTES);
+                    const uint32_t bsm = st + NUM_A * A_TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t bdesc = smem_desc_sw(bsm + kk * 32);
+#pragma unroll
+                        for (int a = 0; a < NUM_A; ++a)
+                            mma_bf16_pair(d0 + (uint32_t)(a * ASTRIDE),
+                                          smem_desc_sw(st + a * A_TILE_BYTES + kk * 32), bdesc, idesc,
+                                          (kb == 0 && kk == 0) ? 0u : 1u);
+                    }
+                    issued_any = true;
+                    mma_commit_pair(smem_u32(&empty_bar[stage]));  // frees the stage in both CTAs
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit_pair(smem_u32(&tfull_bar[acc]));  // accumulator ready in both CTAs
+                if (++acc == ACC) { acc = 0; acc_phase ^= 1; }
+            }
+            if (issued_any) {
+                mma_commit_pair_local(smem_u32(drain_bar));
+                const uint64_t t0 = moe::globaltimer_ns();
+                while (!mbar_try_wait(smem_u32(drain_bar), 0) &&
+                       moe::globaltimer_ns() - t0 < moe::WAIT_LIMIT_NS) {
+                }
+            }
+        }
+    } else if (U > 0 && warp >= 2) {
+        // ================= epilogue: this CTA's tensor memory -> global =================
+        const int q = warp & 3;
+        const int sub = (warp - 2) >> 2;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int slot = 0;
+        uint32_t uphase = 0;
+        while (true) {
+            int u = -1;
+            if (lane == 0 && mbar_wait_cluster(smem_u32(&ufull_bar[slot]), uphase, abort_flag, p.err,
+                                               moe::WAIT_LIMIT_NS)) {
+                u = ring[slot];
+                if (leader)
+                    mbar_arrive(smem_u32(&uempty_bar[slot]));
+                else
+                    mbar_arrive_remote(leader_uempty0 + 8 * slot);
+            }
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (++slot == RING) { slot = 0; uphase ^= 1; }
+            if (u < 0) break;
+            const Unit t = decode_unit<BN, C::FEAT>(u, sched);
+            if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.err,
+                           moe::WAIT_LIMIT_NS))
+                break;
+            tc_fence_after();
+            const int n = t.n0 + (int)rank * BM + q * 32 + lane;
+            const bool n_ok = n < p.N_out;
+            void* out = t.second ? p.out2 : p.out;
+            const uint32_t tbase =
+                tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
+            for (int c0 = 32 * sub; c0 < t.n_tok; c0 += 64) {
+                uint32_t g[32];
+                tmem_ld32(tbase + c0, g);
+                if (MODE == 0) {
+                    uint32_t up[32];
+                    tmem_ld32(tbase + ASTRIDE + c0, up);
+                    tmem_wait_ld();
+                    __nv_bfloat16* H = static_cast<__nv_bfloat16*>(out);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int tok = c0 + j;
+                        if (n_ok && tok < t.n_tok) {
+                            const float gv = __uint_as_float(g[j]);
+                            const float uv = __uint_as_float(up[j]);
+                            const float h = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                            H[(size_t)(t.m_start + tok) * p.N_out + n] = __float2bfloat16_rn(h);
+                        }
+                    }
+                } else {
+                    uint32_t g2[32];
+                    tmem_ld32(tbase + ASTRIDE + c0, g2);
+                    tmem_wait_ld();
+                    const int n2 = n + 2 * BM;  // the second MMA's features
+                    const bool n2_ok = n2 < p.N_out;
+                    float* Y = static_cast<float*>(out);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int tok = c0 + j;
+                        if (tok < t.n_tok) {
+                            float* row = Y + (size_t)(t.m_start + tok) * p.N_out;
+                            if (n_ok) row[n] = __uint_as_float(g[j]);
+                            if (n2_ok) row[n2] = __uint_as_float(g2[j]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(smem_u32(&tempty_bar[acc]));
+                else
+                    mbar_arrive_remote(leader_tempty0 + 8 * acc);
+            }
+            if (++acc == ACC) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // the pair's MMAs and remote arrivals are done
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
 // Self-test of the bounded pipeline wait: an mbarrier that nothing arrives
 // on; the wait must give up and report a timeout.
 __global__ void mbar_probe_kernel(uint64_t limit_ns, uint32_t* err) {
@@ -964,6 +1507,32 @@ int launch(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, const BM
     return moe_host::launch_status();
 }
 
+// The two-SM kernel over CTA pairs: one pair per TPC (half the SMs), or the
+// smallest pair count with the same number of waves when the host knows the
+// units.
+template <int MODE>
+int launch_pair(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, const BMaps& b2,
+                const Params& p, cudaStream_t s, long long units = 0) {
+    static bool attr_done[64] = {};
+    const size_t smem = Cfg2<MODE>::SMEM;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        if (cudaFuncSetAttribute(grouped_gemm_2sm_kernel<MODE>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    int pairs = std::max(1, moe_host::num_sms() / 2);
+    if (MOE_BALANCED_GRID && units > 0) {
+        const long long waves = (units + pairs - 1) / pairs;
+        pairs = (int)((units + waves - 1) / waves);
+    }
+    grouped_gemm_2sm_kernel<MODE><<<2 * pairs, NUM_THREADS, smem, s>>>(a, b, a2, b2, p);
+    return moe_host::launch_status();
+}
+
 }  // namespace
 
 namespace moe_tc {
@@ -1034,14 +1603,21 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
         dense && !two_gu ? (long long)((rows + gu_bn - 1) / gu_bn) * ((I + BM - 1) / BM) : 0;
     const long long dn_units =
         dense && !two_dn ? (long long)((rows + dn_bn - 1) / dn_bn) * ((d + 2 * BM - 1) / (2 * BM)) : 0;
+    // routed launches with 256-token tiles may run on CTA pairs (two-SM
+    // MMAs); not the fused combine's down projection, whose vector-reduction
+    // epilogue is written for the one-SM tile
+    const bool gu_pair = MOE_PAIR_GU && gu_wide && !dense;
+    const bool dn_pair = MOE_PAIR_DN && dn_wide && MOE_DN_BN == 256 && !fc && !dense;
     int rc = MOE_OK;
     if (parts & 1)
-        rc = gu_wide ? launch<0, 256>(a1, b1, a1s, b1s, p1, s, gu_units)
-                     : launch<0, MOE_GU_BN>(a1, b1, a1s, b1s, p1, s, gu_units);
+        rc = gu_pair ? launch_pair<0>(a1, b1, a1s, b1s, p1, s)
+             : gu_wide ? launch<0, 256>(a1, b1, a1s, b1s, p1, s, gu_units)
+                       : launch<0, MOE_GU_BN>(a1, b1, a1s, b1s, p1, s, gu_units);
     if (rc != MOE_OK) return rc;
     if (between && cudaEventRecord(between, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (!(parts & 2)) return MOE_OK;
     if (before_down && cudaStreamWaitEvent(s, before_down, 0) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dn_pair) return launch_pair<1>(a2, b2, a2s, b2s, p2, s);
     return dn_wide ? launch<1, MOE_DN_BN>(a2, b2, a2s, b2s, p2, s, dn_units)
                    : launch<1, 128>(a2, b2, a2s, b2s, p2, s, dn_units);
 }
