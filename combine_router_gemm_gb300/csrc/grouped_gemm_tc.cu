@@ -84,6 +84,11 @@ struct ModeCfg;
 #ifndef MOE_GU_BN
 #define MOE_GU_BN 160
 #endif
+// below this many rows per expert on average, both launches use 32-token
+// tiles (0: never)
+#ifndef MOE_NARROW_ROWS
+#define MOE_NARROW_ROWS 8
+#endif
 #ifndef MOE_DN_BN
 #define MOE_DN_BN 256
 #endif
@@ -1595,10 +1600,14 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     //            (prefill: 1.57 ms vs 2.01 ms with 128).
     const bool gu_wide = (long long)rows >= (long long)MOE_GU_WIDE_ROWS * E;
     const bool dn_wide = (long long)rows >= (long long)MOE_DN_WIDE_ROWS * E;
+    // a few rows per expert (decode): 32-token tiles, whose 36 KB stages let
+    // each SM keep 6 weight-tile pairs in flight instead of 4
+    const bool narrow = MOE_NARROW_ROWS > 0 && (long long)rows < (long long)MOE_NARROW_ROWS * E;
     // a dense problem alone (offsets == NULL, no second problem): the unit
     // counts are known here
     const bool dense = offsets == nullptr;
-    const int gu_bn = gu_wide ? 256 : MOE_GU_BN, dn_bn = dn_wide ? MOE_DN_BN : 128;
+    const int gu_bn = gu_wide ? 256 : narrow ? 32 : MOE_GU_BN;
+    const int dn_bn = dn_wide ? MOE_DN_BN : narrow ? 32 : 128;
     const long long gu_units =
         dense && !two_gu ? (long long)((rows + gu_bn - 1) / gu_bn) * ((I + BM - 1) / BM) : 0;
     const long long dn_units =
@@ -1612,12 +1621,14 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     if (parts & 1)
         rc = gu_pair ? launch_pair<0>(a1, b1, a1s, b1s, p1, s)
              : gu_wide ? launch<0, 256>(a1, b1, a1s, b1s, p1, s, gu_units)
+             : narrow  ? launch<0, 32>(a1, b1, a1s, b1s, p1, s, gu_units)
                        : launch<0, MOE_GU_BN>(a1, b1, a1s, b1s, p1, s, gu_units);
     if (rc != MOE_OK) return rc;
     if (between && cudaEventRecord(between, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (!(parts & 2)) return MOE_OK;
     if (before_down && cudaStreamWaitEvent(s, before_down, 0) != cudaSuccess) return MOE_ERR_CUDA;
     if (dn_pair) return launch_pair<1>(a2, b2, a2s, b2s, p2, s);
+    if (narrow && !dn_wide) return launch<1, 32>(a2, b2, a2s, b2s, p2, s, dn_units);
     return dn_wide ? launch<1, MOE_DN_BN>(a2, b2, a2s, b2s, p2, s, dn_units)
                    : launch<1, 128>(a2, b2, a2s, b2s, p2, s, dn_units);
 }
