@@ -154,6 +154,10 @@ SMALL_BF16 = [
     inputs.MoEConfig("small_dsv3_wide_shared", T=300, d=256, E=16, k=4, I=128, dtype="bf16",
                      score_fn="sigmoid", n_group=4, topk_group=2, routed_scale=2.5,
                      shared_I=256, bias="normal", expert_std=0.06, router_std=0.06),
+    # 512 rows per expert: both routed launches on CTA pairs (256-token tiles);
+    # without a second stream the shared expert's tiles ride in them
+    inputs.MoEConfig("small_pairs_shared", T=2048, d=256, E=8, k=2, I=128, dtype="bf16",
+                     shared_I=128, expert_std=0.06),
 ]
 
 
@@ -258,8 +262,8 @@ FUSED_RAGGED = inputs.MoEConfig("fused_ragged", T=333, d=200, E=12, k=3, I=136, 
                                 shared_I=136, bias="normal", expert_std=0.06, router_std=0.06)
 
 
-@pytest.mark.parametrize("cfg", [SMALL_BF16[0], SMALL_BF16[1], EDGE[0][0], FUSED_RAGGED],
-                         ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [SMALL_BF16[0], SMALL_BF16[1], SMALL_BF16[3], EDGE[0][0],
+                                 FUSED_RAGGED], ids=lambda c: c.name)
 def test_layer_fused_combine(oracle, cfg):
     """The down projection adding its results straight into the output (fp32
     atomics) agrees with the oracle at the bf16 tolerances, and with the
@@ -286,7 +290,8 @@ def test_layer_fused_combine_full_size(oracle):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("cfg", [SMALL_BF16[0], SMALL_BF16[2], inputs.CONFIGS["tiny_fp32"]],
+@pytest.mark.parametrize("cfg", [SMALL_BF16[0], SMALL_BF16[2], SMALL_BF16[3],
+                                 inputs.CONFIGS["tiny_fp32"]],
                          ids=lambda c: c.name)
 def test_layer_cuda_graph_replay(oracle, cfg):
     """The layer recorded into a CUDA graph (both streams) and replayed on new
