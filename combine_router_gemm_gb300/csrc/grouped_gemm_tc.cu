@@ -873,6 +873,10 @@ constexpr int BN2 = 256;  // token tile of a CTA pair (each CTA: 128 rows)
 #ifndef MOE_PAIR_DN
 #define MOE_PAIR_DN 1
 #endif
+// the shared expert's own dense launches on pairs as well
+#ifndef MOE_PAIR_DENSE
+#define MOE_PAIR_DENSE 0
+#endif
 
 template <int MODE>
 struct Cfg2 {
@@ -1615,11 +1619,17 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     // routed launches with 256-token tiles may run on CTA pairs (two-SM
     // MMAs); not the fused combine's down projection, whose vector-reduction
     // epilogue is written for the one-SM tile
-    const bool gu_pair = MOE_PAIR_GU && gu_wide && !dense;
-    const bool dn_pair = MOE_PAIR_DN && dn_wide && MOE_DN_BN == 256 && !fc && !dense;
+    const bool gu_pair = MOE_PAIR_GU && gu_wide && (!dense || MOE_PAIR_DENSE);
+    const bool dn_pair = MOE_PAIR_DN && dn_wide && MOE_DN_BN == 256 && !fc && (!dense || MOE_PAIR_DENSE);
+    // a dense problem alone: its units on pairs (256 features x 256 tokens for
+    // gate/up, 512 x 256 for down), for the balanced grid
+    const long long gu_pair_units =
+        dense && !two_gu ? (long long)((rows + 255) / 256) * ((I + 255) / 256) : 0;
+    const long long dn_pair_units =
+        dense && !two_dn ? (long long)((rows + 255) / 256) * ((d + 511) / 512) : 0;
     int rc = MOE_OK;
     if (parts & 1)
-        rc = gu_pair ? launch_pair<0>(a1, b1, a1s, b1s, p1, s)
+        rc = gu_pair ? launch_pair<0>(a1, b1, a1s, b1s, p1, s, gu_pair_units)
              : gu_wide ? launch<0, 256>(a1, b1, a1s, b1s, p1, s, gu_units)
              : narrow  ? launch<0, 32>(a1, b1, a1s, b1s, p1, s, gu_units)
                        : launch<0, MOE_GU_BN>(a1, b1, a1s, b1s, p1, s, gu_units);
@@ -1627,7 +1637,7 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     if (between && cudaEventRecord(between, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (!(parts & 2)) return MOE_OK;
     if (before_down && cudaStreamWaitEvent(s, before_down, 0) != cudaSuccess) return MOE_ERR_CUDA;
-    if (dn_pair) return launch_pair<1>(a2, b2, a2s, b2s, p2, s);
+    if (dn_pair) return launch_pair<1>(a2, b2, a2s, b2s, p2, s, dn_pair_units);
     if (narrow && !dn_wide) return launch<1, 32>(a2, b2, a2s, b2s, p2, s, dn_units);
     return dn_wide ? launch<1, MOE_DN_BN>(a2, b2, a2s, b2s, p2, s, dn_units)
                    : launch<1, 128>(a2, b2, a2s, b2s, p2, s, dn_units);
