@@ -335,7 +335,7 @@ int moe_combine(const float* y_perm, const int32_t* slot_to_row, const float* to
         (shared && !moe_host::aligned16(shared)))
         return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
-    return moe_launch::combine(y_perm, slot_to_row, topk_w, shared, T, k, d, out, nullptr,
+    return moe_launch::combine(y_perm, T * k, slot_to_row, topk_w, shared, T, k, d, out, nullptr,
                                static_cast<cudaStream_t>(stream));
 }
 
@@ -458,7 +458,7 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     if (rc == MOE_OK && overlap && !merged && cudaStreamWaitEvent(s0, ev_shared, 0) != cudaSuccess)
         rc = MOE_ERR_CUDA;
     if (rc == MOE_OK && !fused)
-        rc = moe_launch::combine(w.yp, w.s2r, w.w, w.ysh, T, k, d, out, w.err, s0);
+        rc = moe_launch::combine(w.yp, T * k, w.s2r, w.w, w.ysh, T, k, d, out, w.err, s0);
     mark(6);
     if (own_events) {
         cudaEventDestroy(ev_start);

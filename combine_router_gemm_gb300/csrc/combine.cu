@@ -18,14 +18,13 @@ constexpr int CB_MAXK = 32;
 template <int KC>
 __global__ void __launch_bounds__(CB_THREADS) combine_kernel(
     const float4* __restrict__ y, const int32_t* __restrict__ slot_to_row,
-    const float* __restrict__ w, const float4* __restrict__ shared, int T, int k_rt, int d4,
+    const float* __restrict__ w, const float4* __restrict__ shared, int rows, int k_rt, int d4,
     float4* __restrict__ out, const uint32_t* err) {
     const int k = KC ? KC : k_rt;
     __shared__ int s_row[CB_MAXK];
     __shared__ float s_w[CB_MAXK];
     __shared__ int s_skip, s_bad;
-    const int t = blockIdx.x;
-    const int rows = T * k;
+    const int t = blockIdx.x;  // token, relative to the arrays passed in
     if (threadIdx.x == 0) {
         s_skip = moe::read_error(err) != 0;
         s_bad = 0;
@@ -81,18 +80,19 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(
 
 namespace moe_launch {
 
-int combine(const float* y, const int32_t* slot_to_row, const float* w, const float* shared, int T,
-            int k, int d, float* out, const uint32_t* err, cudaStream_t s) {
+int combine(const float* y, int rows, const int32_t* slot_to_row, const float* w,
+            const float* shared, int T, int k, int d, float* out, const uint32_t* err,
+            cudaStream_t s) {
     if (k > CB_MAXK) return MOE_ERR_UNSUPPORTED;
     const float4* y4 = reinterpret_cast<const float4*>(y);
     const float4* sh4 = reinterpret_cast<const float4*>(shared);
     float4* o4 = reinterpret_cast<float4*>(out);
     if (k == 8)
-        combine_kernel<8><<<T, CB_THREADS, 0, s>>>(y4, slot_to_row, w, sh4, T, k, d / 4, o4, err);
+        combine_kernel<8><<<T, CB_THREADS, 0, s>>>(y4, slot_to_row, w, sh4, rows, k, d / 4, o4, err);
     else if (k == 2)
-        combine_kernel<2><<<T, CB_THREADS, 0, s>>>(y4, slot_to_row, w, sh4, T, k, d / 4, o4, err);
+        combine_kernel<2><<<T, CB_THREADS, 0, s>>>(y4, slot_to_row, w, sh4, rows, k, d / 4, o4, err);
     else
-        combine_kernel<0><<<T, CB_THREADS, 0, s>>>(y4, slot_to_row, w, sh4, T, k, d / 4, o4, err);
+        combine_kernel<0><<<T, CB_THREADS, 0, s>>>(y4, slot_to_row, w, sh4, rows, k, d / 4, o4, err);
     return moe_host::launch_status();
 }
 

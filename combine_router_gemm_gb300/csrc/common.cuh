@@ -123,6 +123,10 @@ size_t ffn_ws_bytes(int rows, int I, int dtype);
 int grouped_ffn(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
                 const void* w13, const void* w2, int dtype, float* y, void* h_ws, uint32_t* err,
                 cudaStream_t s);
-int combine(const float* y, const int32_t* slot_to_row, const float* w, const float* shared, int T,
-            int k, int d, float* out, const uint32_t* err, cudaStream_t s);
+// out[t] for tokens t of the arrays passed in (slot_to_row, w, shared, out
+// may point into a token range of the layer's); rows = rows of y, which
+// slot_to_row indexes
+int combine(const float* y, int rows, const int32_t* slot_to_row, const float* w,
+            const float* shared, int T, int k, int d, float* out, const uint32_t* err,
+            cudaStream_t s);
 }  // namespace moe_launch

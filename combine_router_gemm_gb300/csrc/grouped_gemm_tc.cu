@@ -1230,6 +1230,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                            moe::globaltimer_ns() - t0 < 10000000ull) {
                     }
                 }
+            } else if (*abort_flag && issued > 0) {
+                // the follower's copies complete on the leader's barriers, which
+                // it cannot wait on: give any still in flight into this CTA's
+                // shared memory a fixed, bounded time (10 ms) to land
+                const uint64_t t0 = moe::globaltimer_ns();
+                while (moe::globaltimer_ns() - t0 < 10000000ull) {
+                }
             }
         }
     } else if (U > 0 && warp == 1) {
