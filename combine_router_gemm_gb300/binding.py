@@ -316,8 +316,9 @@ def moe_layer(args: LayerArgs, out, ws, stream=None, stream2=None):
 
 
 def moe_selftest_bounded_wait(which: int, limit_us: int, ws, stream=None):
-    """Run a wait that nothing signals (0: mbarrier, 1: look-back flag); the
-    kernel must give up after limit_us and flag a timeout in ws."""
+    """Run a wait that nothing signals (0: mbarrier, 1: look-back flag, 2:
+    cluster-scope mbarrier in a two-CTA cluster); the kernel must give up
+    after limit_us and flag a timeout in ws."""
     rc = load().moe_selftest_bounded_wait(which, limit_us, _ptr(ws, None, "ws"),
                                           ws.numel() * ws.element_size(), _stream(stream))
     _check(rc, "moe_selftest_bounded_wait")

@@ -490,13 +490,14 @@ int moe_pack_expert_weights(const void* w13, const void* w2, int E, int d, int I
 
 int moe_selftest_bounded_wait(int which, uint32_t limit_us, void* ws, size_t ws_bytes,
                               void* stream) {
-    if ((which != 0 && which != 1) || limit_us < 1 || limit_us > 1000000) return MOE_ERR_INVALID_ARG;
+    if (which < 0 || which > 2 || limit_us < 1 || limit_us > 1000000) return MOE_ERR_INVALID_ARG;
     if (!ws || !moe_host::aligned16(ws) || ws_bytes < ERR_BYTES + 256) return MOE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, ERR_BYTES + 256, s) != cudaSuccess) return MOE_ERR_CUDA;
     uint32_t* err = static_cast<uint32_t*>(ws);
     const uint64_t ns = 1000ull * limit_us;
     if (which == 0) return moe_tc::mbar_probe(ns, err, s);
+    if (which == 2) return moe_tc::cluster_probe(ns, err, s);
     return moe_launch::lookback_probe(static_cast<char*>(ws) + ERR_BYTES, ns, err, s);
 }
 

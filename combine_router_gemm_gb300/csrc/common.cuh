@@ -93,6 +93,7 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
 int pack_weights(const void* w, int E, int rows, int K, bool pairs, void* out, cudaStream_t s);
 size_t router_ws_bytes(int T, int E, int d);
 int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s);
+int cluster_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s);
 // after_split: recorded once the weight split is done, before the GEMM.
 // presplit: the weight already split ([3,E,d] bf16), or NULL to split it
 // into the workspace first.

@@ -411,6 +411,60 @@ __device__ __forceinline__ Unit decode_unit(int u, const Sched& q) {
     return r;
 }
 
+// The launch's schedule, by one warp: per expert the token tiles of the
+// compute class (at least MOE_COMPUTE_ROWS rows) and of the streaming class,
+// their prefix sums pre_c / pre_s [E+1], and total_units = {all units (-1:
+// inconsistent offsets or an earlier stage failed: no work), compute-stream
+// units, streaming-stream units}.  Inconsistent offsets are reported when
+// `report` is set.
+template <int BN>
+__device__ __forceinline__ void build_schedule(const Params& p, int n_tiles, int U2, int* pre_c,
+                                               int* pre_s, int* total_units, bool report) {
+    const int lane = threadIdx.x & 31, E = p.E;
+    // per-lane chunk of experts, then warp scans of the chunk sums
+    const int per = (E + 31) / 32;
+    const int lo = min(E, lane * per), hi = min(E, lo + per);
+    int sum_c = 0, sum_s = 0;
+    bool bad = false;
+    for (int e = lo; e < hi; ++e) {
+        const int a = p.offsets ? p.offsets[e] : 0;
+        const int b = p.offsets ? p.offsets[e + 1] : p.rows;
+        if (a < 0 || b < a || b > p.rows) bad = true;
+        const int mt = (b - a + BN - 1) / BN;
+        if (b - a >= MOE_COMPUTE_ROWS) sum_c += mt; else sum_s += mt;
+    }
+    int inc_c = sum_c, inc_s = sum_s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int oc = __shfl_up_sync(0xffffffffu, inc_c, off);
+        const int os = __shfl_up_sync(0xffffffffu, inc_s, off);
+        if (lane >= off) {
+            inc_c += oc;
+            inc_s += os;
+        }
+    }
+    int run_c = inc_c - sum_c, run_s = inc_s - sum_s;
+    for (int e = lo; e < hi; ++e) {
+        pre_c[e] = run_c;
+        pre_s[e] = run_s;
+        const int a = p.offsets ? p.offsets[e] : 0;
+        const int b = p.offsets ? p.offsets[e + 1] : p.rows;
+        const int mt = (b - a + BN - 1) / BN;
+        if (b - a >= MOE_COMPUTE_ROWS) run_c += mt; else run_s += mt;
+    }
+    const bool any_bad = __any_sync(0xffffffffu, bad);
+    if (lane == 31) {
+        pre_c[E] = inc_c;
+        pre_s[E] = inc_s;
+        // an earlier stage that failed, or inconsistent offsets: no work
+        const bool fail = any_bad || moe::read_error(p.err);
+        total_units[0] = fail ? -1 : (inc_c + inc_s) * n_tiles + U2;
+        total_units[1] = inc_c * n_tiles + U2;  // compute stream
+        total_units[2] = inc_s * n_tiles;       // streaming stream
+        if (any_bad && report) moe::raise_error(p.err, moe::ERR_BAD_OFFSETS);
+    }
+}
+
 // ---------------------------------------------------------------- the kernel
 
 template <int MODE, int BN_>
@@ -448,50 +502,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int U2 = p.rows2 > 0 ? ((p.rows2 + BN - 1) / BN) * n_tiles : 0;
     int* pre_c = mpre;             // [E+1]
     int* pre_s = mpre + (E + 1);   // [E+1]
-    if (warp == 0) {
-        // per-lane chunk of experts, then warp scans of the chunk sums
-        const int per = (E + 31) / 32;
-        const int lo = min(E, lane * per), hi = min(E, lo + per);
-        int sum_c = 0, sum_s = 0;
-        bool bad = false;
-        for (int e = lo; e < hi; ++e) {
-            const int a = p.offsets ? p.offsets[e] : 0;
-            const int b = p.offsets ? p.offsets[e + 1] : p.rows;
-            if (a < 0 || b < a || b > p.rows) bad = true;
-            const int mt = (b - a + BN - 1) / BN;
-            if (b - a >= MOE_COMPUTE_ROWS) sum_c += mt; else sum_s += mt;
-        }
-        int inc_c = sum_c, inc_s = sum_s;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int oc = __shfl_up_sync(0xffffffffu, inc_c, off);
-            const int os = __shfl_up_sync(0xffffffffu, inc_s, off);
-            if (lane >= off) {
-                inc_c += oc;
-                inc_s += os;
-            }
-        }
-        int run_c = inc_c - sum_c, run_s = inc_s - sum_s;
-        for (int e = lo; e < hi; ++e) {
-            pre_c[e] = run_c;
-            pre_s[e] = run_s;
-            const int a = p.offsets ? p.offsets[e] : 0;
-            const int b = p.offsets ? p.offsets[e + 1] : p.rows;
-            const int mt = (b - a + BN - 1) / BN;
-            if (b - a >= MOE_COMPUTE_ROWS) run_c += mt; else run_s += mt;
-        }
-        const bool any_bad = __any_sync(0xffffffffu, bad);
-        if (lane == 31) {
-            pre_c[E] = inc_c;
-            pre_s[E] = inc_s;
-            // an earlier stage that failed, or inconsistent offsets: no work
-            const bool fail = any_bad || moe::read_error(p.err);
-            total_units[0] = fail ? -1 : (inc_c + inc_s) * n_tiles + U2;
-            total_units[1] = inc_c * n_tiles + U2;  // compute stream
-            total_units[2] = inc_s * n_tiles;       // streaming stream
-            if (any_bad) moe::raise_error(p.err, moe::ERR_BAD_OFFSETS);
-        }
-    }
+    if (warp == 0) build_schedule<BN>(p, n_tiles, U2, pre_c, pre_s, total_units, true);
     if (tid == 0) {
         *abort_flag = 0;
         for (int s = 0; s < STAGES; ++s) {
@@ -1035,48 +1046,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int U2 = p.rows2 > 0 ? ((p.rows2 + BN - 1) / BN) * n_tiles : 0;
     int* pre_c = mpre;
     int* pre_s = mpre + (E + 1);
-    if (warp == 0) {
-        const int per = (E + 31) / 32;
-        const int lo = min(E, lane * per), hi = min(E, lo + per);
-        int sum_c = 0, sum_s = 0;
-        bool bad = false;
-        for (int e = lo; e < hi; ++e) {
-            const int a = p.offsets ? p.offsets[e] : 0;
-            const int b = p.offsets ? p.offsets[e + 1] : p.rows;
-            if (a < 0 || b < a || b > p.rows) bad = true;
-            const int mt = (b - a + BN - 1) / BN;
-            if (b - a >= MOE_COMPUTE_ROWS) sum_c += mt; else sum_s += mt;
-        }
-        int inc_c = sum_c, inc_s = sum_s;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int oc = __shfl_up_sync(0xffffffffu, inc_c, off);
-            const int os = __shfl_up_sync(0xffffffffu, inc_s, off);
-            if (lane >= off) {
-                inc_c += oc;
-                inc_s += os;
-            }
-        }
-        int run_c = inc_c - sum_c, run_s = inc_s - sum_s;
-        for (int e = lo; e < hi; ++e) {
-            pre_c[e] = run_c;
-            pre_s[e] = run_s;
-            const int a = p.offsets ? p.offsets[e] : 0;
-            const int b = p.offsets ? p.offsets[e + 1] : p.rows;
-            const int mt = (b - a + BN - 1) / BN;
-            if (b - a >= MOE_COMPUTE_ROWS) run_c += mt; else run_s += mt;
-        }
-        const bool any_bad = __any_sync(0xffffffffu, bad);
-        if (lane == 31) {
-            pre_c[E] = inc_c;
-            pre_s[E] = inc_s;
-            const bool fail = any_bad || moe::read_error(p.err);
-            total_units[0] = fail ? -1 : (inc_c + inc_s) * n_tiles + U2;
-            total_units[1] = inc_c * n_tiles + U2;
-            total_units[2] = inc_s * n_tiles;
-            if (any_bad && leader) moe::raise_error(p.err, moe::ERR_BAD_OFFSETS);
-        }
-    }
+    if (warp == 0) build_schedule<BN>(p, n_tiles, U2, pre_c, pre_s, total_units, leader);
     if (tid == 0) {
         *abort_flag = 0;
         for (int s = 0; s < STAGES; ++s) {
@@ -1406,6 +1376,26 @@ __global__ void mbar_probe_kernel(uint64_t limit_ns, uint32_t* err) {
     if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, err, limit_ns);
 }
 
+// Self-test of the CTA pair's bounded cluster-scope wait: in a cluster of
+// two, each CTA waits (acquire.cluster, as the pair kernel's ring and
+// accumulator waits do) on a barrier that the peer would arrive on but never
+// does; the waits must give up and report a timeout, then both CTAs meet at
+// the cluster barrier and exit.
+__global__ void __cluster_dims__(2, 1, 1) cluster_probe_kernel(uint64_t limit_ns, uint32_t* err) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    cluster_sync_all();
+    if (threadIdx.x == 0) mbar_wait_cluster(smem_u32(&bar), 0, &abort_flag, err, limit_ns);
+    __syncthreads();
+    cluster_sync_all();
+}
+
 // Router weight split: w = hi + mid + lo with each term the bf16 rounding of
 // what the previous terms leave (every subtraction is exact in fp32; the sum
 // is exact for |w| >= 2^-110, below which bf16's spacing drops the last bits).
@@ -1661,6 +1651,11 @@ int pack_weights(const void* w, int E, int rows, int K, bool pairs, void* out, c
 
 int mbar_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s) {
     mbar_probe_kernel<<<1, 32, 0, s>>>(limit_ns, err);
+    return moe_host::launch_status();
+}
+
+int cluster_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t s) {
+    cluster_probe_kernel<<<2, 32, 0, s>>>(limit_ns, err);
     return moe_host::launch_status();
 }
 

@@ -344,7 +344,9 @@ int moe_check_error(void* ws, void* stream, uint32_t* detail);
  * Self-test of the bounded device waits (failure detection without a fault).
  * Launches one tiny kernel that waits on something nothing will ever signal:
  * which = 0: an mbarrier, as in the grouped-GEMM pipeline; which = 1: a
- * predecessor's look-back flag, as in the dispatch scan.  The wait gives up
+ * predecessor's look-back flag, as in the dispatch scan; which = 2: an
+ * mbarrier with cluster-scope acquire in each CTA of a two-CTA cluster, as
+ * in the CTA-pair grouped GEMM's cross-CTA waits.  The wait gives up
  * after limit_us microseconds (1..1000000) and sets the error word of `ws`
  * (>= 512 bytes, any contents); moe_check_error(ws, ...) then returns
  * MOE_ERR_TIMEOUT.  The kernels of the layer use the same waits with a

@@ -217,3 +217,10 @@ def test_layer_flag_bits(lib):
                     flags=B.LAYER_SHARED_AFTER_ROUTER | 16)
     need = lib.moe_layer_workspace_size(ctypes.byref(a))
     assert lib.moe_layer(ctypes.byref(a), P, P, need, None, None) == B.ERR_INVALID_ARG
+
+
+def test_selftest_rejects(lib):
+    # host-side checks, nothing is launched
+    assert lib.moe_selftest_bounded_wait(3, 1000, P, 4096, None) == B.ERR_INVALID_ARG
+    assert lib.moe_selftest_bounded_wait(2, 0, P, 4096, None) == B.ERR_INVALID_ARG
+    assert lib.moe_selftest_bounded_wait(2, 1000, P, 16, None) == B.ERR_WORKSPACE

@@ -13,7 +13,7 @@ from combine_router_gemm_gb300 import binding as B
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("which", [0, 1], ids=["mbarrier", "lookback"])
+@pytest.mark.parametrize("which", [0, 1, 2], ids=["mbarrier", "lookback", "cluster_mbarrier"])
 def test_bounded_wait_times_out_and_reports(which):
     ws = torch.empty(4096, dtype=torch.uint8, device="cuda")
     t0 = time.perf_counter()
