@@ -888,15 +888,20 @@ constexpr int BN2 = 256;  // token tile of a CTA pair (each CTA: 128 rows)
 #ifndef MOE_PAIR_DENSE
 #define MOE_PAIR_DENSE 0
 #endif
+// routed gate/up with fewer rows per expert (weight streaming) on pairs with
+// 128-token tiles
+#ifndef MOE_PAIR_GU128
+#define MOE_PAIR_GU128 0
+#endif
 
-template <int MODE>
+template <int MODE, int BN_ = BN2>
 struct Cfg2 {
-    static constexpr int BN = BN2;
+    static constexpr int BN = BN_;
     static constexpr int NUM_A = 2;       // weight tiles per CTA and stage
     static constexpr int HB = BN / 2;     // token rows per CTA
     static constexpr int STAGE_BYTES = NUM_A * A_TILE_BYTES + HB * BK * 2;
     static constexpr int STAGES = SMEM_BUDGET / STAGE_BYTES;
-    static constexpr int ASTRIDE = 256;   // TMEM columns between the two accumulators
+    static constexpr int ASTRIDE = BN;    // TMEM columns between the two accumulators
     static constexpr int ACC_COLS = NUM_A * ASTRIDE;
     static constexpr int ACC_STAGES = TMEM_COLS / ACC_COLS;
     // output features per unit: gate/up, 256 features of W1 and the same of
@@ -1009,13 +1014,13 @@ __device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
                  : "memory");
 }
 
-template <int MODE>
+template <int MODE, int BN_ = BN2>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_a,
                             const __grid_constant__ BMaps tm_b,
                             const __grid_constant__ CUtensorMap tm_a2,
                             const __grid_constant__ BMaps tm_b2, const Params p) {
-    using C = Cfg2<MODE>;
+    using C = Cfg2<MODE, BN_>;
     constexpr int STAGES = C::STAGES, NUM_A = C::NUM_A, ACC = C::ACC_STAGES, BN = C::BN;
     constexpr int ACC_COLS = C::ACC_COLS, ASTRIDE = C::ASTRIDE, HB = C::HB;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1516,15 +1521,15 @@ int launch(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, const BM
 // The two-SM kernel over CTA pairs: one pair per TPC (half the SMs), or the
 // smallest pair count with the same number of waves when the host knows the
 // units.
-template <int MODE>
+template <int MODE, int BN = BN2>
 int launch_pair(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, const BMaps& b2,
                 const Params& p, cudaStream_t s, long long units = 0) {
     static bool attr_done[64] = {};
-    const size_t smem = Cfg2<MODE>::SMEM;
+    const size_t smem = Cfg2<MODE, BN>::SMEM;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        if (cudaFuncSetAttribute(grouped_gemm_2sm_kernel<MODE>,
+        if (cudaFuncSetAttribute(grouped_gemm_2sm_kernel<MODE, BN>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
             return MOE_ERR_CUDA;
@@ -1535,7 +1540,7 @@ int launch_pair(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, con
         const long long waves = (units + pairs - 1) / pairs;
         pairs = (int)((units + waves - 1) / waves);
     }
-    grouped_gemm_2sm_kernel<MODE><<<2 * pairs, NUM_THREADS, smem, s>>>(a, b, a2, b2, p);
+    grouped_gemm_2sm_kernel<MODE, BN><<<2 * pairs, NUM_THREADS, smem, s>>>(a, b, a2, b2, p);
     return moe_host::launch_status();
 }
 
@@ -1624,9 +1629,13 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
         dense && !two_gu ? (long long)((rows + 255) / 256) * ((I + 255) / 256) : 0;
     const long long dn_pair_units =
         dense && !two_dn ? (long long)((rows + 255) / 256) * ((d + 511) / 512) : 0;
+    // routed gate/up below the wide threshold (and above the narrow one):
+    // 128-token tiles on CTA pairs instead of 160-token one-SM tiles
+    const bool gu_pair128 = MOE_PAIR_GU128 && !gu_wide && !narrow && !dense;
     int rc = MOE_OK;
     if (parts & 1)
-        rc = gu_pair ? launch_pair<0>(a1, b1, a1s, b1s, p1, s, gu_pair_units)
+        rc = gu_pair128 ? launch_pair<0, 128>(a1, b1, a1s, b1s, p1, s)
+             : gu_pair ? launch_pair<0>(a1, b1, a1s, b1s, p1, s, gu_pair_units)
              : gu_wide ? launch<0, 256>(a1, b1, a1s, b1s, p1, s, gu_units)
              : narrow  ? launch<0, 32>(a1, b1, a1s, b1s, p1, s, gu_units)
                        : launch<0, MOE_GU_BN>(a1, b1, a1s, b1s, p1, s, gu_units);
