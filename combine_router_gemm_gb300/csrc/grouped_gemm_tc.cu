@@ -893,6 +893,11 @@ constexpr int BN2 = 256;  // token tile of a CTA pair (each CTA: 128 rows)
 #ifndef MOE_PAIR_GU128
 #define MOE_PAIR_GU128 0
 #endif
+// token tile of the wide (compute-bound) routed gate/up on pairs: 256, or 128
+// (double-buffered accumulators, more bytes per MMA)
+#ifndef MOE_PAIR_GU_BN
+#define MOE_PAIR_GU_BN 256
+#endif
 
 template <int MODE, int BN_ = BN2>
 struct Cfg2 {
@@ -1635,7 +1640,9 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     int rc = MOE_OK;
     if (parts & 1)
         rc = gu_pair128 ? launch_pair<0, 128>(a1, b1, a1s, b1s, p1, s)
-             : gu_pair ? launch_pair<0>(a1, b1, a1s, b1s, p1, s, gu_pair_units)
+             : gu_pair ? (MOE_PAIR_GU_BN == 128 ? launch_pair<0, 128>(a1, b1, a1s, b1s, p1, s)
+                                                : launch_pair<0>(a1, b1, a1s, b1s, p1, s,
+                                                                 gu_pair_units))
              : gu_wide ? launch<0, 256>(a1, b1, a1s, b1s, p1, s, gu_units)
              : narrow  ? launch<0, 32>(a1, b1, a1s, b1s, p1, s, gu_units)
                        : launch<0, MOE_GU_BN>(a1, b1, a1s, b1s, p1, s, gu_units);
