@@ -58,16 +58,16 @@ NOMINAL_BF16_TFLOPS = 2250.0
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the routed
 # gate/up GEMM per launch, from ncu captures of this kernel source.  Reported
 # as null once the kernel source no longer matches the captured one.
-TRAFFIC = {"source_sha256": "e710a7b0c5314dc22c9cfc19b847d2d2eca8e570ce1f227968f68e2f157d98ac",
+TRAFFIC = {"source_sha256": "1becd5224923b45202fb70e201b67e28efc5261c54ec945b6dd4d8aff17d1f02",
            # routed gate/up launch on tile-major weights (the shared expert
            # runs on the second stream): dsv3_prefill_e32 from an ncu capture
-           # of the 32-expert case (dram__bytes_read.sum 1.950709e9 +
-           # dram__bytes_write.sum 0.018255e9); dsv3_prefill is that capture
+           # of the 32-expert case (dram__bytes_read.sum 1.950619e9 +
+           # dram__bytes_write.sum 0.017895e9); dsv3_prefill is that capture
            # scaled by the units processed (8x the experts at the same rows
            # per expert, 8x the tokens), the workload being too large for a
            # multi-metric capture
-           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.968964e9,
-                                            "dsv3_prefill": 8 * 1.968964e9}}
+           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.968514e9,
+                                            "dsv3_prefill": 8 * 1.968514e9}}
 
 
 def peaks():

@@ -1523,24 +1523,47 @@ int launch(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, const BM
     return moe_host::launch_status();
 }
 
-// The two-SM kernel over CTA pairs: one pair per TPC (half the SMs), or the
-// smallest pair count with the same number of waves when the host knows the
-// units.
+// Two-CTA clusters of the pair kernel that the current device can hold at
+// once (queried once per device; 0 if none or the query fails, in which case
+// the one-SM kernel runs instead).  The kernel's shared-memory limit is set
+// on the same first use.
+template <int MODE, int BN = BN2>
+int pair_capacity() {
+    static int cap[64];
+    static bool done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!done[dev]) {
+        const size_t smem = Cfg2<MODE, BN>::SMEM;
+        int n = 0;
+        if (cudaFuncSetAttribute(grouped_gemm_2sm_kernel<MODE, BN>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * std::max(1, moe_host::num_sms() / 2));
+            cfg.blockDim = dim3(NUM_THREADS);
+            cfg.dynamicSmemBytes = smem;
+            // the cluster size (2) is the kernel's own (__cluster_dims__)
+            if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_2sm_kernel<MODE, BN>, &cfg) !=
+                cudaSuccess)
+                n = 0;
+        }
+        cudaGetLastError();  // a refused query leaves no error behind
+        cap[dev] = n;
+        done[dev] = true;
+    }
+    return cap[dev];
+}
+
+// The two-SM kernel over CTA pairs: as many pairs as the device holds at once
+// (one per TPC: half the SMs), or the smallest pair count with the same
+// number of waves when the host knows the units.
 template <int MODE, int BN = BN2>
 int launch_pair(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, const BMaps& b2,
                 const Params& p, cudaStream_t s, long long units = 0) {
-    static bool attr_done[64] = {};
     const size_t smem = Cfg2<MODE, BN>::SMEM;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        if (cudaFuncSetAttribute(grouped_gemm_2sm_kernel<MODE, BN>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        if (dev >= 0 && dev < 64) attr_done[dev] = true;
-    }
-    int pairs = std::max(1, moe_host::num_sms() / 2);
+    int pairs = std::min(std::max(1, moe_host::num_sms() / 2), pair_capacity<MODE, BN>());
+    if (pairs < 1) return MOE_ERR_UNSUPPORTED;
     if (MOE_BALANCED_GRID && units > 0) {
         const long long waves = (units + pairs - 1) / pairs;
         pairs = (int)((units + waves - 1) / waves);
@@ -1626,8 +1649,10 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     // routed launches with 256-token tiles may run on CTA pairs (two-SM
     // MMAs); not the fused combine's down projection, whose vector-reduction
     // epilogue is written for the one-SM tile
-    const bool gu_pair = MOE_PAIR_GU && gu_wide && (!dense || MOE_PAIR_DENSE);
-    const bool dn_pair = MOE_PAIR_DN && dn_wide && MOE_DN_BN == 256 && !fc && (!dense || MOE_PAIR_DENSE);
+    const bool gu_pair = MOE_PAIR_GU && gu_wide && (!dense || MOE_PAIR_DENSE) &&
+                         (MOE_PAIR_GU_BN == 128 ? pair_capacity<0, 128>() : pair_capacity<0>()) > 0;
+    const bool dn_pair = MOE_PAIR_DN && dn_wide && MOE_DN_BN == 256 && !fc &&
+                         (!dense || MOE_PAIR_DENSE) && pair_capacity<1>() > 0;
     // a dense problem alone: its units on pairs (256 features x 256 tokens for
     // gate/up, 512 x 256 for down), for the balanced grid
     const long long gu_pair_units =
@@ -1636,7 +1661,8 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
         dense && !two_dn ? (long long)((rows + 255) / 256) * ((d + 511) / 512) : 0;
     // routed gate/up below the wide threshold (and above the narrow one):
     // 128-token tiles on CTA pairs instead of 160-token one-SM tiles
-    const bool gu_pair128 = MOE_PAIR_GU128 && !gu_wide && !narrow && !dense;
+    const bool gu_pair128 =
+        MOE_PAIR_GU128 && !gu_wide && !narrow && !dense && pair_capacity<0, 128>() > 0;
     int rc = MOE_OK;
     if (parts & 1)
         rc = gu_pair128 ? launch_pair<0, 128>(a1, b1, a1s, b1s, p1, s)
