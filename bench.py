@@ -631,8 +631,9 @@ def run_ours(args, cfg):
             "metric": METRIC, "value": m["value"], "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": warm, "ms_per_step": m["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
-            "config": {**config_dict(cfg), "expert_weights": "tile-major, packed once at layer "
-                       "construction" if not args.row_major_weights else "row-major"},
+            "config": config_dict(cfg),
+            "expert_weights": ("tile-major, packed once at layer construction"
+                               if not args.row_major_weights else "row-major"),
             "roofline": m["roofline"], "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": m["clocks"], "stages": m["stages"],
             "active_experts": m["active_experts"], "wall_s_timed": m["wall_s_timed"],
