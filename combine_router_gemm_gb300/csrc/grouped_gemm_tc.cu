@@ -35,7 +35,10 @@
 //  * Routed launches with 256-token tiles run the same design on CTA pairs
 //    (grouped_gemm_2sm_kernel below, tcgen05.mma.cta_group::2): two weight
 //    tiles and half the token tile per SM and stage, a quarter fewer bytes
-//    per multiply-add than the one-SM tile.
+//    per multiply-add than the one-SM tile.  The compute-bound down
+//    projection runs two such pairs per cluster on neighbouring feature
+//    tiles: each half of the token tile is loaded by one pair and multicast
+//    to both, so an SM loads a quarter of the token tile per stage.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -898,6 +901,25 @@ constexpr int BN2 = 256;  // token tile of a CTA pair (each CTA: 128 rows)
 #ifndef MOE_PAIR_GU128
 #define MOE_PAIR_GU128 0
 #endif
+// clusters of two CTA pairs sharing the token tile by multicast, for the
+// compute-bound routed launches (0: one pair per cluster).  The GPU holds 36
+// clusters of four (144 SMs) against 76 pairs (152), so the quarter fewer
+// token-tile bytes per SM must pay for 5% fewer SMs.  Measured on one box,
+// one pair per cluster vs two: Mixtral down 0.566 -> 0.556 ms, gate/up
+// 1.17 -> 1.22 ms (slower); on the power-capped DeepSeek-V3 Zipf(1.2)
+// T=16384 layer (~512 rows per expert) the layer took 10.03 ms with one
+// pair and 10.07-10.14 ms with two on the down projection.  So the down
+// projection only, from 768 rows per expert.
+#ifndef MOE_QUAD_GU
+#define MOE_QUAD_GU 0
+#endif
+#ifndef MOE_QUAD_DN
+#define MOE_QUAD_DN 1
+#endif
+// rows per expert from which the down projection takes two pairs per cluster
+#ifndef MOE_QUAD_DN_ROWS
+#define MOE_QUAD_DN_ROWS 768
+#endif
 // token tile of the wide (compute-bound) routed gate/up on pairs: 256, or 128
 // (double-buffered accumulators, more bytes per MMA)
 #ifndef MOE_PAIR_GU_BN
@@ -998,6 +1020,19 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// The same, multicast: the tile lands at this shared-memory offset in every
+// CTA of `mask`, and each destination's bytes complete on the barrier at the
+// given offset in that destination's pair leader
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map,
+                                                    uint32_t bar_cluster, int x, int y,
+                                                    uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes."
+        "multicast::cluster.cta_group::2 [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster), "h"(mask)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b,
                                               uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -1008,9 +1043,9 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a, uint6
         : "memory");
 }
 
-// commit the leader's MMAs so far to the barrier at this offset in both CTAs
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
-    const uint16_t mask = 3;
+// commit the leader's MMAs so far to the barrier at this offset in the CTAs
+// of `mask` (cluster ranks)
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
         "[%0], %1;" ::"r"(bar),
@@ -1024,8 +1059,14 @@ __device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
                  : "memory");
 }
 
-template <int MODE, int BN_ = BN2>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+// CL: CTAs per cluster.  2: one pair.  4: two pairs that work on neighbouring
+// feature tiles of the same token tile; each half of the token tile is loaded
+// once, by the two pairs in turn (alternate k-blocks), and multicast to the
+// CTA of the same rank in both pairs, so that each SM loads a quarter of the
+// tile per stage instead of half; a stage is released only when both pairs
+// have consumed it.
+template <int MODE, int BN_ = BN2, int CL = 2>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_a,
                             const __grid_constant__ BMaps tm_b,
                             const __grid_constant__ CUtensorMap tm_a2,
@@ -1050,23 +1091,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     int* total_units = reinterpret_cast<int*>(tmem_slot + 2);
     volatile int* ring = reinterpret_cast<volatile int*>(tmem_slot + 5);  // [RING]
     int* mpre = reinterpret_cast<int*>(smem + (size_t)STAGES * C::STAGE_BYTES + 256);
+    static_assert(CL == 2 || CL == 4, "one or two CTA pairs per cluster");
+    constexpr int FEATC = (CL / 2) * C::FEAT;  // output features per cluster unit
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t rank = cluster_rank();
-    const bool leader = rank == 0;
-    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const uint32_t crank = cluster_rank();      // rank in the cluster
+    const uint32_t rank = crank & 1u;           // rank in the CTA pair
+    const uint32_t pl = crank & ~1u;            // the pair leader's cluster rank
+    const int cpair = (int)(crank >> 1);        // which pair of the cluster
+    const bool leader = rank == 0;              // pair leader (issues the MMAs)
+    const bool cleader = crank == 0;            // cluster leader (claims units)
+    const int cluster = blockIdx.x / CL, nclusters = gridDim.x / CL;
 
-    // ---- schedule (both CTAs compute the same tables) ----
+    // ---- schedule (every CTA computes the same tables) ----
     const int E = p.E;
-    const int n_tiles = (p.N_out + C::FEAT - 1) / C::FEAT;
+    const int n_tiles = (p.N_out + FEATC - 1) / FEATC;
     const int U2 = p.rows2 > 0 ? ((p.rows2 + BN - 1) / BN) * n_tiles : 0;
     int* pre_c = mpre;
     int* pre_s = mpre + (E + 1);
-    if (warp == 0) build_schedule<BN>(p, n_tiles, U2, pre_c, pre_s, total_units, leader);
+    if (warp == 0) build_schedule<BN>(p, n_tiles, U2, pre_c, pre_s, total_units, cleader);
     if (tid == 0) {
         *abort_flag = 0;
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
-            mbar_init(smem_u32(&empty_bar[s]), 1);
+            // released by the commits of every pair leader of the cluster
+            mbar_init(smem_u32(&empty_bar[s]), CL / 2);
         }
         for (int a = 0; a < ACC; ++a) {
             mbar_init(smem_u32(&tfull_bar[a]), 1);
@@ -1075,9 +1123,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         mbar_init(smem_u32(drain_bar), 1);
         for (int r = 0; r < RING; ++r) {
             mbar_init(smem_u32(&ufull_bar[r]), 1);
-            // leader: its MMA thread and epilogue warps, the follower's
-            // producer and epilogue warps
-            mbar_init(smem_u32(&uempty_bar[r]), 2 + 2 * NUM_EPI_WARPS);
+            // cluster leader: every pair leader's MMA thread, every CTA's
+            // epilogue warps, the other CTAs' producers
+            mbar_init(smem_u32(&uempty_bar[r]), CL / 2 + CL * NUM_EPI_WARPS + (CL - 1));
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tm_a);
@@ -1097,7 +1145,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive
+    cluster_sync_all();  // every CTA's barriers initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int U = total_units[0];
@@ -1112,10 +1160,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int num_kb = (p.K + BK - 1) / BK;
     const Sched sched{pre_c, pre_s, offs, E, n_tiles, total_units[0], total_units[1],
                       total_units[2], U2, p.rows2};
-    // the leader's barriers as cluster addresses (for the follower's arrivals)
-    const uint32_t leader_full0 = peer_addr(smem_u32(&full_bar[0]), 0);
-    const uint32_t leader_tempty0 = peer_addr(smem_u32(&tempty_bar[0]), 0);
-    const uint32_t leader_uempty0 = peer_addr(smem_u32(&uempty_bar[0]), 0);
+    // the pair leader's and the cluster leader's barriers as cluster addresses
+    const uint32_t leader_full0 = peer_addr(smem_u32(&full_bar[0]), pl);
+    const uint32_t leader_tempty0 = peer_addr(smem_u32(&tempty_bar[0]), pl);
+    const uint32_t cl_uempty0 = peer_addr(smem_u32(&uempty_bar[0]), 0);
 
     if (U > 0 && warp == 0) {
         // ================= TMA producer (one thread per CTA) =================
@@ -1125,39 +1173,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             int slot = 0;
             uint32_t uphase = 0;
             long issued = 0;
-            const uint32_t f_ring0 = peer_addr(smem_u32((const void*)&ring[0]), 1);
-            const uint32_t f_ufull0 = peer_addr(smem_u32(&ufull_bar[0]), 1);
-            int u = pair;
+            int u = cluster;
             while (true) {
-                if (leader) {
-                    // publish u (or the end, -1) to both CTAs
+                if (cleader) {
+                    // publish u (or the end, -1) to every CTA of the cluster
                     if (!mbar_wait_cluster(smem_u32(&uempty_bar[slot]), uphase ^ 1, abort_flag,
                                            p.err, moe::WAIT_LIMIT_NS))
                         break;
                     const int v = (u >= U || *abort_flag) ? -1 : u;
                     ring[slot] = v;
-                    st_remote_u32(f_ring0 + 4 * slot, v);
+#pragma unroll
+                    for (int r = 1; r < CL; ++r)
+                        st_remote_u32(peer_addr(smem_u32((const void*)&ring[slot]), r), v);
                     mbar_arrive(smem_u32(&ufull_bar[slot]));
-                    mbar_arrive_remote(f_ufull0 + 8 * slot);
+#pragma unroll
+                    for (int r = 1; r < CL; ++r)
+                        mbar_arrive_remote(peer_addr(smem_u32(&ufull_bar[slot]), r));
                     u = v;
                 } else {
                     if (!mbar_wait_cluster(smem_u32(&ufull_bar[slot]), uphase, abort_flag, p.err,
                                            moe::WAIT_LIMIT_NS))
                         break;
                     u = ring[slot];
-                    mbar_arrive_remote(leader_uempty0 + 8 * slot);
+                    mbar_arrive_remote(cl_uempty0 + 8 * slot);
                 }
                 if (++slot == RING) { slot = 0; uphase ^= 1; }
                 if (u < 0) break;
-                const int next = leader ? npairs + (int)atomicAdd(p.work, 1u) : 0;
-                const Unit t = decode_unit<BN, C::FEAT>(u, sched);
+                const int next = cleader ? nclusters + (int)atomicAdd(p.work, 1u) : 0;
+                const Unit t = decode_unit<BN, FEATC>(u, sched);
                 const CUtensorMap* ma = t.second ? &tm_a2 : &tm_a;
                 const CUtensorMap* mb = t.second ? tm_b2.m : tm_b.m;
                 const int bn = (t.n_tok + 31) & ~31;  // MMA N: a multiple of 32
                 const int hb = bn / 2;                // token rows per CTA
                 const int nbox = (hb + B_BOX - 1) / B_BOX;
                 const uint32_t cta_bytes = NUM_A * A_TILE_BYTES + nbox * B_BOX_BYTES;
-                const int a_row = (t.second ? 0 : t.e * p.a_rows) + t.n0 + (int)rank * BM;
+                const int a_row =
+                    (t.second ? 0 : t.e * p.a_rows) + t.n0 + cpair * C::FEAT + (int)rank * BM;
                 const int a_step = MODE == 1 ? C::A_STEP_DN : p.a_step;
                 const int m0 = t.m_start + (int)rank * hb;
                 bool ok = true;
@@ -1185,12 +1236,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                             tma_load_2d_pair(smem_u32(st + a * A_TILE_BYTES), ma, fb_pair, x, y);
                     }
                     uint8_t* bdst = st + NUM_A * A_TILE_BYTES;
+                    // two pairs: this CTA's half of the token tile comes from
+                    // the pairs in turn, multicast to the same rank of both
+                    const bool load_b = CL == 2 || (kb & 1) == cpair;
+                    const uint16_t bmask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
                     int row = 0;
 #pragma unroll
                     for (int lv = 2; lv >= 0; --lv) {  // boxes of 128/64/32 rows
                         const int h = B_BOX << lv;
-                        if (h <= HB && (nbox * B_BOX - row) >= h) {
-                            if (leader)
+                        if (load_b && h <= HB && (nbox * B_BOX - row) >= h) {
+                            if (CL == 4)
+                                tma_load_2d_pair_mc(smem_u32(bdst + row * BK * 2), mb + lv, fb_pair,
+                                                    kx, m0 + row, bmask);
+                            else if (leader)
                                 tma_load_2d(smem_u32(bdst + row * BK * 2), mb + lv, fb, kx,
                                             m0 + row);
                             else
@@ -1203,9 +1261,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                if (leader) u = next;
+                if (cleader) u = next;
             }
-            if (*abort_flag && leader) {
+            if (*abort_flag && leader && CL == 2) {
                 // let the copies of this stage ring land before the CTA exits
                 for (int i = 0; i < STAGES && issued > 0; ++i, --issued) {
                     if (stage == 0) { stage = STAGES; phase ^= 1; }
@@ -1216,16 +1274,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             } else if (*abort_flag && issued > 0) {
-                // the follower's copies complete on the leader's barriers, which
-                // it cannot wait on: give any still in flight into this CTA's
-                // shared memory a fixed, bounded time (10 ms) to land
+                // copies that complete on another CTA's barriers (the follower's,
+                // and every multicast one) cannot be waited on here: give any
+                // still in flight into shared memory a fixed, bounded time
+                // (10 ms) to land
                 const uint64_t t0 = moe::globaltimer_ns();
                 while (moe::globaltimer_ns() - t0 < 10000000ull) {
                 }
             }
         }
     } else if (U > 0 && warp == 1) {
-        // ================= MMA issuer (one thread of the leader) =================
+        // ================= MMA issuer (one thread of each pair leader) =================
         if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
@@ -1234,15 +1293,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             bool issued_any = false;
             int slot = 0;
             uint32_t uphase = 0;
+            // stage releases go to every CTA of the cluster (each may hold
+            // token rows this pair reads); accumulators to this pair's two
+            const uint16_t all_mask = (uint16_t)((1u << CL) - 1u);
+            const uint16_t pair_mask = (uint16_t)(3u << (2 * cpair));
             while (!*abort_flag) {
-                if (!mbar_wait(smem_u32(&ufull_bar[slot]), uphase, abort_flag, p.err,
-                               moe::WAIT_LIMIT_NS))
+                if (!mbar_wait_cluster(smem_u32(&ufull_bar[slot]), uphase, abort_flag, p.err,
+                                       moe::WAIT_LIMIT_NS))
                     break;
                 const int u = ring[slot];
-                mbar_arrive(smem_u32(&uempty_bar[slot]));
+                if (cleader)
+                    mbar_arrive(smem_u32(&uempty_bar[slot]));
+                else
+                    mbar_arrive_remote(cl_uempty0 + 8 * slot);
                 if (++slot == RING) { slot = 0; uphase ^= 1; }
                 if (u < 0) break;
-                const Unit t = decode_unit<BN, C::FEAT>(u, sched);
+                const Unit t = decode_unit<BN, FEATC>(u, sched);
                 const int bn = (t.n_tok + 31) & ~31;
                 // M = 256 over the pair (bits 24-28: M / 16), N = bn
                 const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) |
@@ -1272,11 +1338,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                                           (kb == 0 && kk == 0) ? 0u : 1u);
                     }
                     issued_any = true;
-                    mma_commit_pair(smem_u32(&empty_bar[stage]));  // frees the stage in both CTAs
+                    mma_commit_pair(smem_u32(&empty_bar[stage]), all_mask);  // stage consumed
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                mma_commit_pair(smem_u32(&tfull_bar[acc]));  // accumulator ready in both CTAs
+                mma_commit_pair(smem_u32(&tfull_bar[acc]), pair_mask);  // accumulator ready
                 if (++acc == ACC) { acc = 0; acc_phase ^= 1; }
             }
             if (issued_any) {
@@ -1300,20 +1366,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             if (lane == 0 && mbar_wait_cluster(smem_u32(&ufull_bar[slot]), uphase, abort_flag, p.err,
                                                moe::WAIT_LIMIT_NS)) {
                 u = ring[slot];
-                if (leader)
+                if (cleader)
                     mbar_arrive(smem_u32(&uempty_bar[slot]));
                 else
-                    mbar_arrive_remote(leader_uempty0 + 8 * slot);
+                    mbar_arrive_remote(cl_uempty0 + 8 * slot);
             }
             u = __shfl_sync(0xffffffffu, u, 0);
             if (++slot == RING) { slot = 0; uphase ^= 1; }
             if (u < 0) break;
-            const Unit t = decode_unit<BN, C::FEAT>(u, sched);
+            const Unit t = decode_unit<BN, FEATC>(u, sched);
             if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.err,
                            moe::WAIT_LIMIT_NS))
                 break;
             tc_fence_after();
-            const int n = t.n0 + (int)rank * BM + q * 32 + lane;
+            const int n = t.n0 + cpair * C::FEAT + (int)rank * BM + q * 32 + lane;
             const bool n_ok = n < p.N_out;
             void* out = t.second ? p.out2 : p.out;
             const uint32_t tbase =
@@ -1532,7 +1598,7 @@ int launch(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, const BM
 // once (queried once per device; 0 if none or the query fails, in which case
 // the one-SM kernel runs instead).  The kernel's shared-memory limit is set
 // on the same first use.
-template <int MODE, int BN = BN2>
+template <int MODE, int BN = BN2, int CL = 2>
 int pair_capacity() {
     static int cap[64];
     static bool done[64] = {};
@@ -1541,15 +1607,15 @@ int pair_capacity() {
     if (!done[dev]) {
         const size_t smem = Cfg2<MODE, BN>::SMEM;
         int n = 0;
-        if (cudaFuncSetAttribute(grouped_gemm_2sm_kernel<MODE, BN>,
+        if (cudaFuncSetAttribute(grouped_gemm_2sm_kernel<MODE, BN, CL>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(2 * std::max(1, moe_host::num_sms() / 2));
+            cfg.gridDim = dim3(CL * std::max(1, moe_host::num_sms() / CL));
             cfg.blockDim = dim3(NUM_THREADS);
             cfg.dynamicSmemBytes = smem;
-            // the cluster size (2) is the kernel's own (__cluster_dims__)
-            if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_2sm_kernel<MODE, BN>, &cfg) !=
+            // the cluster size (CL) is the kernel's own (__cluster_dims__)
+            if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_2sm_kernel<MODE, BN, CL>, &cfg) !=
                 cudaSuccess)
                 n = 0;
         }
@@ -1563,17 +1629,17 @@ int pair_capacity() {
 // The two-SM kernel over CTA pairs: as many pairs as the device holds at once
 // (one per TPC: half the SMs), or the smallest pair count with the same
 // number of waves when the host knows the units.
-template <int MODE, int BN = BN2>
+template <int MODE, int BN = BN2, int CL = 2>
 int launch_pair(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, const BMaps& b2,
                 const Params& p, cudaStream_t s, long long units = 0) {
     const size_t smem = Cfg2<MODE, BN>::SMEM;
-    int pairs = std::min(std::max(1, moe_host::num_sms() / 2), pair_capacity<MODE, BN>());
-    if (pairs < 1) return MOE_ERR_UNSUPPORTED;
+    int clusters = std::min(std::max(1, moe_host::num_sms() / CL), pair_capacity<MODE, BN, CL>());
+    if (clusters < 1) return MOE_ERR_UNSUPPORTED;
     if (MOE_BALANCED_GRID && units > 0) {
-        const long long waves = (units + pairs - 1) / pairs;
-        pairs = (int)((units + waves - 1) / waves);
+        const long long waves = (units + clusters - 1) / clusters;
+        clusters = (int)((units + waves - 1) / waves);
     }
-    grouped_gemm_2sm_kernel<MODE, BN><<<2 * pairs, NUM_THREADS, smem, s>>>(a, b, a2, b2, p);
+    grouped_gemm_2sm_kernel<MODE, BN, CL><<<CL * clusters, NUM_THREADS, smem, s>>>(a, b, a2, b2, p);
     return moe_host::launch_status();
 }
 
@@ -1658,6 +1724,12 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
                          (MOE_PAIR_GU_BN == 128 ? pair_capacity<0, 128>() : pair_capacity<0>()) > 0;
     const bool dn_pair = MOE_PAIR_DN && dn_wide && MOE_DN_BN == 256 && !fc &&
                          (!dense || MOE_PAIR_DENSE) && pair_capacity<1>() > 0;
+    // two pairs per cluster sharing the token tile (down projection from
+    // MOE_QUAD_DN_ROWS rows per expert)
+    const bool gu_quad = MOE_QUAD_GU && gu_pair && MOE_PAIR_GU_BN == 256 &&
+                         pair_capacity<0, BN2, 4>() > 0;
+    const bool dn_quad = MOE_QUAD_DN && dn_pair && (long long)rows >= (long long)MOE_QUAD_DN_ROWS * E &&
+                         pair_capacity<1, BN2, 4>() > 0;
     // a dense problem alone: its units on pairs (256 features x 256 tokens for
     // gate/up, 512 x 256 for down), for the balanced grid
     const long long gu_pair_units =
@@ -1671,6 +1743,7 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     int rc = MOE_OK;
     if (parts & 1)
         rc = gu_pair128 ? launch_pair<0, 128>(a1, b1, a1s, b1s, p1, s)
+             : gu_quad ? launch_pair<0, BN2, 4>(a1, b1, a1s, b1s, p1, s)
              : gu_pair ? (MOE_PAIR_GU_BN == 128 ? launch_pair<0, 128>(a1, b1, a1s, b1s, p1, s)
                                                 : launch_pair<0>(a1, b1, a1s, b1s, p1, s,
                                                                  gu_pair_units))
@@ -1681,6 +1754,7 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     if (between && cudaEventRecord(between, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (!(parts & 2)) return MOE_OK;
     if (before_down && cudaStreamWaitEvent(s, before_down, 0) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dn_quad) return launch_pair<1, BN2, 4>(a2, b2, a2s, b2s, p2, s);
     if (dn_pair) return launch_pair<1>(a2, b2, a2s, b2s, p2, s, dn_pair_units);
     if (narrow && !dn_wide) return launch<1, 32>(a2, b2, a2s, b2s, p2, s, dn_units);
     return dn_wide ? launch<1, MOE_DN_BN>(a2, b2, a2s, b2s, p2, s, dn_units)

@@ -158,3 +158,21 @@ def test_grouped_ffn_bf16_mixed_classes_wide_tiles(oracle):
     n = int(offsets[-1])
     ref = oracle.grouped_ffn(np_(x), np_(offsets), np_(w13), np_(w2), round_h=True)
     assert_bf16_close(np_(y)[:n], ref, "mixed classes")
+
+
+def test_grouped_ffn_bf16_two_pair_clusters_ragged(oracle):
+    """At least 768 rows per expert on average: the down projection runs on
+    clusters of two CTA pairs (1024 output features per cluster, the token
+    tile multicast to both pairs).  d = 1160 leaves the second feature tile
+    with 136 valid features (the second pair has none), and the token tiles
+    end ragged (900 = 3*256 + 132, 1700 = 6*256 + 164) beside an empty
+    expert; d is also a K tail for gate/up (18 K-blocks + 8)."""
+    E, d, I, counts = 3, 1160, 320, [900, 0, 1700]
+    assert sum(counts) >= 768 * E
+    x, offsets, w13, w2 = make_case(E, d, I, counts, torch.bfloat16, seed=31)
+    y = run_ffn(x, offsets, w13, w2)
+    torch.cuda.synchronize()
+    n = int(offsets[-1])
+    ref = oracle.grouped_ffn(np_(x), np_(offsets), np_(w13), np_(w2), round_h=True)
+    assert_bf16_close(np_(y)[:n], ref, "two-pair clusters")
+    assert rel_fro(np_(y)[:n], ref) < 2e-3
