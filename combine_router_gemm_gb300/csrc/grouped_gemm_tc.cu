@@ -32,7 +32,8 @@
 //  * Every mbarrier wait is bounded (about 1 s); on expiry the kernel sets the
 //    error word, waits briefly for its own copies and MMAs in flight, frees
 //    tensor memory and returns.
-//  * Routed launches with 256-token tiles run the same design on CTA pairs
+//  * Routed launches with 256-token tiles, and routed gate/up launches with
+//    160-token tiles, run the same design on CTA pairs
 //    (grouped_gemm_2sm_kernel below, tcgen05.mma.cta_group::2): two weight
 //    tiles and half the token tile per SM and stage, a quarter fewer bytes
 //    per multiply-add than the one-SM tile.  The compute-bound down
@@ -157,8 +158,10 @@ __host__ __device__ __forceinline__ int packed_tile(int rt, int kb, int num_kb, 
 
 // Tensor maps of one activation matrix with token boxes of 32, 64, 128 and
 // 256 rows (index = log2(rows / 32)).
+// token-tile maps: boxes of 32, 64, 128 and 256 rows, then one of 16 rows
+// (for CTA pairs, whose half tiles are multiples of 16 rows)
 struct BMaps {
-    CUtensorMap m[4];
+    CUtensorMap m[5];
 };
 
 struct Params {
@@ -901,6 +904,13 @@ constexpr int BN2 = 256;  // token tile of a CTA pair (each CTA: 128 rows)
 #ifndef MOE_PAIR_GU128
 #define MOE_PAIR_GU128 0
 #endif
+// the same with 160-token tiles (80 rows per CTA, exact 64 + 16-row boxes;
+// 5 stages of 42 KB per SM, 160 KB of weight tiles in flight instead of the
+// one-SM tile's 128 KB).  DeepSeek-V3 prefill, same box, three repetitions:
+// routed gate/up 2.267-2.271 ms vs 2.282-2.284 ms on one SM.
+#ifndef MOE_PAIR_GU160
+#define MOE_PAIR_GU160 1
+#endif
 // clusters of two CTA pairs sharing the token tile by multicast, for the
 // compute-bound routed launches (0: one pair per cluster).  The GPU holds 36
 // clusters of four (144 SMs) against 76 pairs (152), so the quarter fewer
@@ -933,7 +943,9 @@ struct Cfg2 {
     static constexpr int HB = BN / 2;     // token rows per CTA
     static constexpr int STAGE_BYTES = NUM_A * A_TILE_BYTES + HB * BK * 2;
     static constexpr int STAGES = SMEM_BUDGET / STAGE_BYTES;
-    static constexpr int ASTRIDE = BN;    // TMEM columns between the two accumulators
+    // TMEM columns between the two accumulators (each starts on a 128-column
+    // boundary)
+    static constexpr int ASTRIDE = (BN + 127) / 128 * 128;
     static constexpr int ACC_COLS = NUM_A * ASTRIDE;
     static constexpr int ACC_STAGES = TMEM_COLS / ACC_COLS;
     // output features per unit: gate/up, 256 features of W1 and the same of
@@ -944,7 +956,7 @@ struct Cfg2 {
     static constexpr int A_STEP_DN = 2 * BM;
     static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + sizeof(int) * 2 * (MAX_E + 1);
     static_assert(STAGES >= 2 && ACC_COLS <= TMEM_COLS && ACC_STAGES >= 1, "tile does not fit");
-    static_assert(HB % B_BOX == 0, "half tile must be whole boxes");
+    static_assert(HB % (B_BOX / 2) == 0, "half tile must be whole 16-row boxes");
     static_assert(SMEM + 64 <= (size_t)SMEM_LIMIT, "shared memory over the per-CTA limit");
     // barriers + tensor-memory slot + flags + ring must fit the 256-byte area
     static_assert((2 * STAGES + 2 * ACC_STAGES + 1 + 2 * RING) * 8 + 4 * (5 + RING) <= 256,
@@ -1129,10 +1141,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tm_a);
-        for (int i = 0; i < 4; ++i) tma_prefetch_desc(&tm_b.m[i]);
+        for (int i = 0; i < 5; ++i) tma_prefetch_desc(&tm_b.m[i]);
         if (p.rows2 > 0) {
             tma_prefetch_desc(&tm_a2);
-            for (int i = 0; i < 4; ++i) tma_prefetch_desc(&tm_b2.m[i]);
+            for (int i = 0; i < 5; ++i) tma_prefetch_desc(&tm_b2.m[i]);
         }
     }
     if (warp == 1) {
@@ -1204,9 +1216,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 const CUtensorMap* ma = t.second ? &tm_a2 : &tm_a;
                 const CUtensorMap* mb = t.second ? tm_b2.m : tm_b.m;
                 const int bn = (t.n_tok + 31) & ~31;  // MMA N: a multiple of 32
-                const int hb = bn / 2;                // token rows per CTA
-                const int nbox = (hb + B_BOX - 1) / B_BOX;
-                const uint32_t cta_bytes = NUM_A * A_TILE_BYTES + nbox * B_BOX_BYTES;
+                const int hb = bn / 2;                // token rows per CTA, a multiple of 16
+                const uint32_t cta_bytes = NUM_A * A_TILE_BYTES + hb * BK * 2;
                 const int a_row =
                     (t.second ? 0 : t.e * p.a_rows) + t.n0 + cpair * C::FEAT + (int)rank * BM;
                 const int a_step = MODE == 1 ? C::A_STEP_DN : p.a_step;
@@ -1240,19 +1251,22 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     // the pairs in turn, multicast to the same rank of both
                     const bool load_b = CL == 2 || (kb & 1) == cpair;
                     const uint16_t bmask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
+                    // exactly hb rows, in boxes of 128/64/32/16 rows (hb / 16
+                    // <= 8, so each box size is needed at most once)
                     int row = 0;
 #pragma unroll
-                    for (int lv = 2; lv >= 0; --lv) {  // boxes of 128/64/32 rows
-                        const int h = B_BOX << lv;
-                        if (load_b && h <= HB && (nbox * B_BOX - row) >= h) {
+                    for (int lv = 3; lv >= 0; --lv) {
+                        const int h = (B_BOX / 2) << lv;
+                        if (load_b && h <= HB && hb - row >= h) {
+                            const CUtensorMap* mbox = lv == 0 ? mb + 4 : mb + (lv - 1);
                             if (CL == 4)
-                                tma_load_2d_pair_mc(smem_u32(bdst + row * BK * 2), mb + lv, fb_pair,
+                                tma_load_2d_pair_mc(smem_u32(bdst + row * BK * 2), mbox, fb_pair,
                                                     kx, m0 + row, bmask);
                             else if (leader)
-                                tma_load_2d(smem_u32(bdst + row * BK * 2), mb + lv, fb, kx,
+                                tma_load_2d(smem_u32(bdst + row * BK * 2), mbox, fb, kx,
                                             m0 + row);
                             else
-                                tma_load_2d_pair(smem_u32(bdst + row * BK * 2), mb + lv, fb_pair,
+                                tma_load_2d_pair(smem_u32(bdst + row * BK * 2), mbox, fb_pair,
                                                  kx, m0 + row);
                             row += h;
                         }
@@ -1556,7 +1570,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 bool make_bmaps(BMaps* m, const void* base, uint64_t rows, uint64_t cols) {
     for (int i = 0; i < 4; ++i)
         if (!make_map(&m->m[i], base, rows, cols, (uint32_t)(B_BOX << i))) return false;
-    return true;
+    return make_map(&m->m[4], base, rows, cols, (uint32_t)(B_BOX / 2));
 }
 
 #ifndef MOE_BALANCED_GRID
@@ -1696,11 +1710,12 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     // rate (k-blocks in flight per SM) / (load latency), so the tile trades
     // stages against passes over the weights: every token tile of an expert
     // is one more pass over its weight tiles (from L2 after the first).
-    //   gate/up: 160 rows below 384 rows per expert (4 stages of 52 KB; one
-    //            pass for experts of up to 160 rows; single-buffered
-    //            accumulator pair), else 256.  Measured on DeepSeek-V3
-    //            prefill: 2.38 ms with 160, 2.45 ms with 128 (4 stages,
-    //            double-buffered), 2.85 ms with 256 (3 stages);
+    //   gate/up: 160 rows below 384 rows per expert (one-SM tile: 4 stages
+    //            of 52 KB; on CTA pairs 5 of 42 KB per SM; one pass for
+    //            experts of up to 160 rows; single-buffered accumulator
+    //            pair), else 256.  Measured on DeepSeek-V3 prefill (one SM,
+    //            row-major weights): 2.38 ms with 160, 2.45 ms with 128 (4
+    //            stages, double-buffered), 2.85 ms with 256 (3 stages);
     //   down:    128 only below 32 rows per expert (decode), else 256
     //            (prefill: 1.57 ms vs 2.01 ms with 128).
     const bool gu_wide = (long long)rows >= (long long)MOE_GU_WIDE_ROWS * E;
@@ -1737,12 +1752,16 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     const long long dn_pair_units =
         dense && !two_dn ? (long long)((rows + 255) / 256) * ((d + 511) / 512) : 0;
     // routed gate/up below the wide threshold (and above the narrow one):
-    // 128-token tiles on CTA pairs instead of 160-token one-SM tiles
+    // 160-token tiles on CTA pairs (or, off by default, 128-token ones)
+    // instead of 160-token one-SM tiles
     const bool gu_pair128 =
         MOE_PAIR_GU128 && !gu_wide && !narrow && !dense && pair_capacity<0, 128>() > 0;
+    const bool gu_pair160 = MOE_PAIR_GU160 && !gu_wide && !narrow && !dense && MOE_GU_BN == 160 &&
+                            pair_capacity<0, 160>() > 0;
     int rc = MOE_OK;
     if (parts & 1)
         rc = gu_pair128 ? launch_pair<0, 128>(a1, b1, a1s, b1s, p1, s)
+             : gu_pair160 ? launch_pair<0, 160>(a1, b1, a1s, b1s, p1, s)
              : gu_quad ? launch_pair<0, BN2, 4>(a1, b1, a1s, b1s, p1, s)
              : gu_pair ? (MOE_PAIR_GU_BN == 128 ? launch_pair<0, 128>(a1, b1, a1s, b1s, p1, s)
                                                 : launch_pair<0>(a1, b1, a1s, b1s, p1, s,
