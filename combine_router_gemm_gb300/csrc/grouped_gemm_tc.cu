@@ -64,6 +64,18 @@ constexpr int B_BOX_BYTES = B_BOX * BK * 2;    // 4 KB
 constexpr int NUM_EPI_WARPS = 8;  // two per 32-lane quarter of tensor memory
 constexpr int RING = 4;           // unit indices in flight from producer to consumers
 constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS);
+// epilogue warps of the one-SM kernel per mode (gate/up, down, router): a
+// multiple of 4, each warp reaching one 32-lane quarter of tensor memory.
+// Its gate/up runs the shared expert beside the router and top-k, whose
+// blocks must fit beside it: with 16 warps the route stage of the
+// DeepSeek-V3 Zipf layer grew from 0.29 to 0.76 ms and the prefill layer
+// from 3.94 to 4.00 ms, so 8.
+#ifndef MOE_EPI1_GU
+#define MOE_EPI1_GU 8
+#endif
+__host__ __device__ constexpr int epi1_warps(int mode) { return mode == 0 ? MOE_EPI1_GU : NUM_EPI_WARPS; }
+__host__ __device__ constexpr int threads1(int mode) { return 32 * (2 + epi1_warps(mode)); }
+static_assert(MOE_EPI1_GU % 4 == 0 && MOE_EPI1_GU >= 4, "whole quarters of tensor memory");
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 1024;
 
@@ -479,12 +491,13 @@ __device__ __forceinline__ void build_schedule(const Params& p, int n_tiles, int
 // ---------------------------------------------------------------- the kernel
 
 template <int MODE, int BN_>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(threads1(MODE), 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a,
                            const __grid_constant__ BMaps tm_b,
                            const __grid_constant__ CUtensorMap tm_a2,
                            const __grid_constant__ BMaps tm_b2, const Params p) {
     using C = Cfg<MODE, BN_>;
+    constexpr int EPI1 = epi1_warps(MODE);
     constexpr int STAGES = C::STAGES, NUM_A = C::NUM_A, ACC = C::ACC_STAGES, BN = C::BN;
     constexpr int ACC_COLS = C::ACC_COLS, ASTRIDE = C::ASTRIDE;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -522,12 +535,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int a = 0; a < ACC; ++a) {
             mbar_init(smem_u32(&tfull_bar[a]), 1);
-            mbar_init(smem_u32(&tempty_bar[a]), NUM_EPI_WARPS);
+            mbar_init(smem_u32(&tempty_bar[a]), EPI1);
         }
         mbar_init(smem_u32(drain_bar), 1);
         for (int r = 0; r < RING; ++r) {
             mbar_init(smem_u32(&ufull_bar[r]), 1);
-            mbar_init(smem_u32(&uempty_bar[r]), 1 + NUM_EPI_WARPS);
+            mbar_init(smem_u32(&uempty_bar[r]), 1 + EPI1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tm_a);
@@ -717,8 +730,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (U > 0 && warp >= 2) {
         // ================= epilogue: tensor memory -> global =================
-        // warps 2..9: quarter q = warp % 4 of the 128 TMEM lanes (hardware
-        // rule), the two warps of a quarter take alternate 32-token chunks
+        // warps 2..: quarter q = warp % 4 of the 128 TMEM lanes (hardware
+        // rule), the warps of a quarter take its 32-token chunks in turn
         const int q = warp & 3;
         const int sub = (warp - 2) >> 2;
         int acc = 0;
@@ -748,7 +761,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                        (size_t)(u % KS) * p.rows * p.N_out * sizeof(float);
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
-            for (int c0 = 32 * sub; c0 < t.n_tok; c0 += 64) {
+            for (int c0 = 32 * sub; c0 < t.n_tok; c0 += 32 * (EPI1 / 4)) {
                 uint32_t g[32];
                 tmem_ld32(tbase + c0, g);
                 if (MODE == 0) {
@@ -887,6 +900,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // meet at a cluster barrier before tensor memory is freed and they exit.
 
 constexpr int BN2 = 256;  // token tile of a CTA pair (each CTA: 128 rows)
+// epilogue warps of a CTA in a pair, per mode: a multiple of 4 (each warp
+// reaches one 32-lane quarter of tensor memory; the warps of a quarter take
+// its 32-token column chunks in turn).  The accumulator pair fills tensor
+// memory, so the MMAs of the next unit wait for the drain: the SwiGLU drain
+// (two accumulators, two MUFU operations per output) is latency-bound with
+// two warps per scheduler.  Measured (same box, two repetitions, 8 / 12 / 16
+// warps): Mixtral routed gate/up 1.171-1.181 / 1.136 / 1.107-1.114 ms, Zipf
+// (DeepSeek-V3, T=16384) 5.13 / 5.00 / 4.96-4.97 ms; the down projection's
+// fp32 drain gained nothing (Zipf 3.26 / 3.24 / 3.28-3.29 ms).
+#ifndef MOE_EPI2_GU
+#define MOE_EPI2_GU 16
+#endif
+#ifndef MOE_EPI2_DN
+#define MOE_EPI2_DN 8
+#endif
+__host__ __device__ constexpr int epi2_warps(int mode) { return mode == 0 ? MOE_EPI2_GU : MOE_EPI2_DN; }
+__host__ __device__ constexpr int threads2(int mode) { return 32 * (2 + epi2_warps(mode)); }
+static_assert(MOE_EPI2_GU % 4 == 0 && MOE_EPI2_DN % 4 == 0 && MOE_EPI2_GU >= 4 && MOE_EPI2_DN >= 4,
+              "whole quarters of tensor memory");
 
 // routed launches with 256-token tiles on CTA pairs (two-SM MMAs)
 #ifndef MOE_PAIR_GU
@@ -1078,12 +1110,13 @@ __device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
 // tile per stage instead of half; a stage is released only when both pairs
 // have consumed it.
 template <int MODE, int BN_ = BN2, int CL = 2>
-__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(threads2(MODE), 1)
     grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tm_a,
                             const __grid_constant__ BMaps tm_b,
                             const __grid_constant__ CUtensorMap tm_a2,
                             const __grid_constant__ BMaps tm_b2, const Params p) {
     using C = Cfg2<MODE, BN_>;
+    constexpr int EPI2 = epi2_warps(MODE);
     constexpr int STAGES = C::STAGES, NUM_A = C::NUM_A, ACC = C::ACC_STAGES, BN = C::BN;
     constexpr int ACC_COLS = C::ACC_COLS, ASTRIDE = C::ASTRIDE, HB = C::HB;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1130,14 +1163,14 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
         for (int a = 0; a < ACC; ++a) {
             mbar_init(smem_u32(&tfull_bar[a]), 1);
-            mbar_init(smem_u32(&tempty_bar[a]), 2 * NUM_EPI_WARPS);
+            mbar_init(smem_u32(&tempty_bar[a]), 2 * EPI2);
         }
         mbar_init(smem_u32(drain_bar), 1);
         for (int r = 0; r < RING; ++r) {
             mbar_init(smem_u32(&ufull_bar[r]), 1);
             // cluster leader: every pair leader's MMA thread, every CTA's
             // epilogue warps, the other CTAs' producers
-            mbar_init(smem_u32(&uempty_bar[r]), CL / 2 + CL * NUM_EPI_WARPS + (CL - 1));
+            mbar_init(smem_u32(&uempty_bar[r]), CL / 2 + CL * EPI2 + (CL - 1));
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tm_a);
@@ -1398,7 +1431,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             void* out = t.second ? p.out2 : p.out;
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
-            for (int c0 = 32 * sub; c0 < t.n_tok; c0 += 64) {
+            for (int c0 = 32 * sub; c0 < t.n_tok; c0 += 32 * (EPI2 / 4)) {
                 uint32_t g[32];
                 tmem_ld32(tbase + c0, g);
                 if (MODE == 0) {
@@ -1604,7 +1637,7 @@ int launch(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, const BM
         const long long waves = (units + sms - 1) / sms;
         grid = (int)((units + waves - 1) / waves);
     }
-    grouped_gemm_tc_kernel<MODE, BN><<<grid, NUM_THREADS, smem, s>>>(a, b, a2, b2, p);
+    grouped_gemm_tc_kernel<MODE, BN><<<grid, threads1(MODE), smem, s>>>(a, b, a2, b2, p);
     return moe_host::launch_status();
 }
 
@@ -1626,7 +1659,7 @@ int pair_capacity() {
                                  (int)smem) == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(CL * std::max(1, moe_host::num_sms() / CL));
-            cfg.blockDim = dim3(NUM_THREADS);
+            cfg.blockDim = dim3(threads2(MODE));
             cfg.dynamicSmemBytes = smem;
             // the cluster size (CL) is the kernel's own (__cluster_dims__)
             if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_2sm_kernel<MODE, BN, CL>, &cfg) !=
@@ -1653,7 +1686,8 @@ int launch_pair(const CUtensorMap& a, const BMaps& b, const CUtensorMap& a2, con
         const long long waves = (units + clusters - 1) / clusters;
         clusters = (int)((units + waves - 1) / waves);
     }
-    grouped_gemm_2sm_kernel<MODE, BN, CL><<<CL * clusters, NUM_THREADS, smem, s>>>(a, b, a2, b2, p);
+    grouped_gemm_2sm_kernel<MODE, BN, CL><<<CL * clusters, threads2(MODE), smem, s>>>(a, b, a2, b2,
+                                                                                      p);
     return moe_host::launch_status();
 }
 
