@@ -58,16 +58,16 @@ NOMINAL_BF16_TFLOPS = 2250.0
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the routed
 # gate/up GEMM per launch, from ncu captures of this kernel source.  Reported
 # as null once the kernel source no longer matches the captured one.
-TRAFFIC = {"source_sha256": "500c6f1f759e137af29246e171007aaca4dfcd01e8b4317e2e0cb65cbbfdf1f4",
+TRAFFIC = {"source_sha256": "4cfd4b61e2d94194488671e7bff257af4a4c640ba6d47fed03077f7d95119974",
            # routed gate/up launch on tile-major weights (the shared expert
            # runs on the second stream): dsv3_prefill_e32 from an ncu capture
-           # of the 32-expert case (dram__bytes_read.sum 1.951505e9 +
-           # dram__bytes_write.sum 0.017957e9); dsv3_prefill is that capture
+           # of the 32-expert case (dram__bytes_read.sum 1.950732e9 +
+           # dram__bytes_write.sum 0.018297e9); dsv3_prefill is that capture
            # scaled by the units processed (8x the experts at the same rows
            # per expert, 8x the tokens), the workload being too large for a
            # multi-metric capture
-           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.969462e9,
-                                            "dsv3_prefill": 8 * 1.969462e9}}
+           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.969029e9,
+                                            "dsv3_prefill": 8 * 1.969029e9}}
 
 
 def peaks():
