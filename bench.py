@@ -34,9 +34,12 @@ UNIT = "tokens/s"
 L2_FLUSH_BYTES = 512 << 20
 
 
-def launches_per_step(cfg, two_streams: bool, fused: bool = False, presplit: bool = False) -> int:
+def launches_per_step(cfg, two_streams: bool, fused: bool = False, presplit: bool = False,
+                      split: bool = False) -> int:
     """Our kernels per moe_layer call."""
     n = 4  # top-k, count+scan, permute, router GEMM
+    if split and cfg.E >= 2:
+        n += 2  # the permute and the routed gate/up in two expert halves
     if not fused:
         n += 1  # combine
     if cfg.dtype == "bf16" and not presplit:
@@ -516,7 +519,8 @@ def make_layer(cfg, args, inp):
     from combine_router_gemm_gb300 import binding as B
     return B.MoELayer(inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"],
                       inp["w2_sh"], B.cfg_from(cfg), cfg.T, overlap=not args.no_overlap,
-                      fused_combine=args.fused_combine, pack_weights=not args.row_major_weights)
+                      fused_combine=args.fused_combine, pack_weights=not args.row_major_weights,
+                      split_dispatch=getattr(args, "split_dispatch", False))
 
 
 # the other workloads timed beside the headline one (N = 1), each with the
@@ -626,7 +630,8 @@ def run_ours(args, cfg):
         extras = extra_workloads(args, pk, flush, names)
 
     if rank == 0:
-        launches = launches_per_step(cfg, m["two_streams"], args.fused_combine, presplit) * K
+        launches = launches_per_step(cfg, m["two_streams"], args.fused_combine, presplit,
+                                     args.split_dispatch) * K
         line = {
             "metric": METRIC, "value": m["value"], "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": warm, "ms_per_step": m["ms_per_step"], "higher_is_better": True,
@@ -634,6 +639,8 @@ def run_ours(args, cfg):
             "config": config_dict(cfg),
             "expert_weights": ("tile-major, packed once at layer construction"
                                if not args.row_major_weights else "row-major"),
+            "dispatch": ("permute of the upper expert half on a second stream beside the "
+                         "lower half's gate/up" if args.split_dispatch else "one pass"),
             "roofline": m["roofline"], "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": m["clocks"], "stages": m["stages"],
             "active_experts": m["active_experts"], "wall_s_timed": m["wall_s_timed"],
@@ -670,6 +677,9 @@ def main():
                     help="keep the expert weights row-major (no tile-major packing)")
     ap.add_argument("--fused-combine", action="store_true",
                     help="add the down projection's results straight into the output (atomics)")
+    ap.add_argument("--split-dispatch", action="store_true",
+                    help="permute the upper half of the experts on a second stream beside the "
+                         "lower half's gate/up")
     args = ap.parse_args()
     from combine_router_gemm_gb300 import inputs
     cfg = inputs.CONFIGS[args.config]

@@ -56,9 +56,10 @@ class LayerArgs(ctypes.Structure):
 LAYER_FUSED_COMBINE = 1
 LAYER_PACKED_WEIGHTS = 2
 LAYER_SHARED_AFTER_ROUTER = 4
+LAYER_SPLIT_DISPATCH = 8
 
 LAYER_EVENTS = 7
-LAYER_SYNC_EVENTS = 2
+LAYER_SYNC_EVENTS = 4
 
 
 _lib = None
@@ -383,18 +384,24 @@ class MoELayer:
     depends on it).  Allocation happens only here, in PyTorch, never in the
     library.  With ``pack_weights`` (the default) the expert weights are
     copied once into the tile-major layouts the grouped GEMMs stream fastest,
-    where the shapes allow it; the layer then holds those copies.
+    where the shapes allow it; the layer then holds those copies.  With
+    ``split_dispatch`` the permute of the upper half of the experts runs on a
+    second stream beside the lower half's gate/up (MOE_LAYER_SPLIT_DISPATCH).
     """
 
     def __init__(self, w_router, bias, w13, w2, w13_sh, w2_sh, cfg: RouteCfg, T: int,
                  overlap: bool = True, fused_combine: bool = False, pack_weights: bool = True,
-                 split_router: bool = True):
+                 split_router: bool = True, split_dispatch: bool = False):
         self.cfg = cfg
         self.T = T
         dev = w13.device
         d = w13.shape[2]
         I_sh = w2_sh.shape[1] if w2_sh is not None else 0
+        if split_dispatch and (w13.dtype != torch.bfloat16 or fused_combine):
+            raise ValueError("split_dispatch needs bf16 weights and no fused combine")
         self.flags = LAYER_FUSED_COMBINE if fused_combine else 0
+        if split_dispatch:
+            self.flags |= LAYER_SPLIT_DISPATCH
         self.packed = pack_weights and packable(w13, w2, w13_sh, w2_sh)
         if self.packed:
             p13, p2 = torch.empty_like(w13), torch.empty_like(w2)
@@ -415,8 +422,9 @@ class MoELayer:
                           _dtype_code(w13), cfg, None, None, None, None, None, self.flags)
         self.ws_bytes = moe_layer_workspace_size(sizes)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
-        self.stream2 = torch.cuda.Stream(device=dev) if overlap and w13_sh is not None else None
-        # the two events that fork and join the second stream, made once
+        self.stream2 = (torch.cuda.Stream(device=dev)
+                        if (overlap and w13_sh is not None) or split_dispatch else None)
+        # the events that fork and join the second stream, made once
         self.sync_events = ([torch.cuda.Event() for _ in range(LAYER_SYNC_EVENTS)]
                             if self.stream2 is not None else None)
 

@@ -35,7 +35,7 @@ namespace {
 // Workspace header: the error word, then zeroed counters of the grouped
 // GEMMs' dynamic unit schedule (one per launch that may be in flight).
 constexpr size_t ERR_BYTES = 256;
-constexpr int CTR_ROUTER = 1, CTR_FFN = 2 /* +1 */, CTR_SHARED = 4 /* +1 */;
+constexpr int CTR_ROUTER = 1, CTR_FFN = 2 /* +1 */, CTR_SHARED = 4 /* +1 */, CTR_FFN_HI = 6;
 constexpr size_t HDR_CLEAR = 64;  // bytes of the header cleared per call
 unsigned* ctr(void* ws, int i) { return static_cast<unsigned*>(ws) + i; }
 
@@ -206,8 +206,11 @@ int check_layer(const moe_layer_args* a) {
     for (const void* o : outs)
         if (o && !moe_host::aligned16(o)) return MOE_ERR_INVALID_ARG;
     if (a->flags & ~(MOE_LAYER_FUSED_COMBINE | MOE_LAYER_PACKED_WEIGHTS |
-                     MOE_LAYER_SHARED_AFTER_ROUTER))
+                     MOE_LAYER_SHARED_AFTER_ROUTER | MOE_LAYER_SPLIT_DISPATCH))
         return MOE_ERR_INVALID_ARG;
+    if ((a->flags & MOE_LAYER_SPLIT_DISPATCH) &&
+        (a->dtype != MOE_BF16 || (a->flags & MOE_LAYER_FUSED_COMBINE)))
+        return MOE_ERR_UNSUPPORTED;
     if ((a->flags & MOE_LAYER_PACKED_WEIGHTS) &&
         (a->dtype != MOE_BF16 || a->I % 128 != 0 || a->d % 256 != 0 || a->I_sh % 128 != 0))
         return MOE_ERR_UNSUPPORTED;
@@ -355,6 +358,12 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     const int T = a->T, d = a->d, I = a->I, E = a->route.num_experts, k = a->route.top_k;
     cudaStream_t s0 = static_cast<cudaStream_t>(stream);
     cudaStream_t s1 = static_cast<cudaStream_t>(stream2);
+    const bool two_streams = s1 && s1 != s0;
+    const bool fused = a->flags & MOE_LAYER_FUSED_COMBINE;
+    if ((a->flags & MOE_LAYER_SPLIT_DISPATCH) && (!two_streams || a->dtype != MOE_BF16 || fused))
+        return MOE_ERR_UNSUPPORTED;
+    // dispatch overlapped with the gate/up of the lower half of the experts
+    const bool split = (a->flags & MOE_LAYER_SPLIT_DISPATCH) && E >= 2;
     if (cudaMemsetAsync(w.err, 0, HDR_CLEAR, s0) != cudaSuccess) return MOE_ERR_CUDA;
     if (T == 0) {
         // an empty batch: every expert gets zero rows
@@ -378,26 +387,29 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     // which adds them into the output.  Without stream2, bf16 with I_sh == I
     // puts both of its halves into the routed launches; other shapes run it
     // as launches of its own on the main stream.
-    const bool two_streams = s1 && s1 != s0;
     const bool fits = sh && a->dtype == MOE_BF16 && a->I_sh == I;
     const bool merged = fits && (!two_streams || (a->flags & MOE_LAYER_FUSED_COMBINE));
     moe_tc::SharedExpert shx{a->x, T, a->w13_sh, a->w2_sh, w.hsh, w.ysh,
                              /*in_gate_up=*/!two_streams, /*in_down=*/true};
-    cudaEvent_t ev_start = nullptr, ev_shared = nullptr;
     const bool overlap = sh && two_streams;
-    // fork/join events: the caller's, else two made (and destroyed) here
-    const bool own_events = overlap && !a->sync_events;
-    if (overlap && a->sync_events) {
-        ev_start = static_cast<cudaEvent_t>(a->sync_events[0]);
-        ev_shared = static_cast<cudaEvent_t>(a->sync_events[1]);
-        if (!ev_start || !ev_shared) return MOE_ERR_INVALID_ARG;
+    // fork/join events: the caller's, else made (and destroyed) here.  [0]
+    // the shared expert's start, [1] its end, [2] counts and offsets done,
+    // [3] the upper half's permute done.
+    cudaEvent_t ev[MOE_LAYER_SYNC_EVENTS] = {};
+    const int n_ev = split ? 4 : overlap ? 2 : 0;
+    const bool own_events = n_ev > 0 && !a->sync_events;
+    for (int i = 0; i < n_ev; ++i) {
+        if (own_events) {
+            if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
+                for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+                return MOE_ERR_CUDA;
+            }
+        } else {
+            ev[i] = static_cast<cudaEvent_t>(a->sync_events[i]);
+            if (!ev[i]) return MOE_ERR_INVALID_ARG;
+        }
     }
-    if (own_events &&
-        (cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) != cudaSuccess ||
-         cudaEventCreateWithFlags(&ev_shared, cudaEventDisableTiming) != cudaSuccess)) {
-        if (ev_start) cudaEventDestroy(ev_start);
-        return MOE_ERR_CUDA;
-    }
+    cudaEvent_t ev_start = ev[0], ev_shared = ev[1], ev_count = ev[2], ev_upper = ev[3];
     // the shared expert on stream2 starts when the router GEMM is launched
     // (bf16): its CTAs take the SMs that the router's single wave of tiles
     // leaves idle, then continue beside the top-k and dispatch kernels.
@@ -411,12 +423,68 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
                        a->w_router_split, a->flags & MOE_LAYER_SHARED_AFTER_ROUTER);
     mark(1);
     mark(2);
-    const bool fused = a->flags & MOE_LAYER_FUSED_COMBINE;
     // fused combine: the output is accumulated into, so it starts at zero;
     // on stream2 (before the shared expert, which the down launch waits for)
     // when given, so that the main stream does not pay for it
     const bool zero_on_s1 = fused && merged && overlap;
     const bool packed = a->flags & MOE_LAYER_PACKED_WEIGHTS;
+    const int Ea = E / 2;  // split: experts [0, Ea) on `stream` first
+    if (split) {
+        // counts and offsets, then the upper half's permute (and the shared
+        // expert after it) on stream2 while the lower half's permute and
+        // gate/up run here
+        if (rc == MOE_OK)
+            rc = moe_launch::dispatch(w.idx, a->x, a->dtype, T, d, k, E, w.counts, w.offsets,
+                                      w.s2r, w.r2t, w.xp, w.disp, w.err, s0, nullptr, nullptr,
+                                      /*parts=*/1);
+        if (rc == MOE_OK && cudaEventRecord(ev_count, s0) != cudaSuccess) rc = MOE_ERR_CUDA;
+        if (rc == MOE_OK && cudaStreamWaitEvent(s1, ev_count, 0) != cudaSuccess) rc = MOE_ERR_CUDA;
+        if (rc == MOE_OK)
+            rc = moe_launch::dispatch(w.idx, a->x, a->dtype, T, d, k, E, w.counts, w.offsets,
+                                      w.s2r, w.r2t, w.xp, w.disp, w.err, s1, nullptr, nullptr,
+                                      /*parts=*/2, Ea, E);
+        if (rc == MOE_OK && cudaEventRecord(ev_upper, s1) != cudaSuccess) rc = MOE_ERR_CUDA;
+        if (rc == MOE_OK && overlap)
+            rc = run_ffn(a->x, nullptr, 1, T, d, a->I_sh, a->w13_sh, a->w2_sh, a->dtype, w.ysh,
+                         w.hsh, w.err, ctr(w.err, CTR_SHARED), s1, nullptr, packed);
+        if (rc == MOE_OK && overlap && cudaEventRecord(ev_shared, s1) != cudaSuccess)
+            rc = MOE_ERR_CUDA;
+        if (rc == MOE_OK)
+            rc = moe_launch::dispatch(w.idx, a->x, a->dtype, T, d, k, E, w.counts, w.offsets,
+                                      w.s2r, w.r2t, w.xp, w.disp, w.err, s0, nullptr, nullptr,
+                                      /*parts=*/2, 0, Ea);
+        mark(3);
+        // gate/up of each half (experts' weights are contiguous per expert in
+        // both layouts), the tile chosen as for all E experts; then the down
+        // projection over all of them
+        const size_t w13_e = (size_t)2 * I * d * 2, w2_e = (size_t)d * I * 2;
+        const char* w13c = static_cast<const char*>(a->w13);
+        const char* w2c = static_cast<const char*>(a->w2);
+        if (rc == MOE_OK)
+            rc = moe_tc::grouped_ffn_bf16(w.xp, w.offsets, Ea, T * k, d, I, a->w13, a->w2, w.yp,
+                                          w.h, w.err, ctr(w.err, CTR_FFN), s0, nullptr, nullptr,
+                                          nullptr, /*parts=*/1, nullptr, packed, E);
+        if (rc == MOE_OK && cudaStreamWaitEvent(s0, ev_upper, 0) != cudaSuccess) rc = MOE_ERR_CUDA;
+        if (rc == MOE_OK)
+            rc = moe_tc::grouped_ffn_bf16(w.xp, w.offsets + Ea, E - Ea, T * k, d, I,
+                                          w13c + (size_t)Ea * w13_e, w2c + (size_t)Ea * w2_e,
+                                          w.yp, w.h, w.err, ctr(w.err, CTR_FFN_HI), s0, nullptr,
+                                          nullptr, nullptr, /*parts=*/1, nullptr, packed, E);
+        mark(4);
+        if (rc == MOE_OK)
+            rc = moe_tc::grouped_ffn_bf16(w.xp, w.offsets, E, T * k, d, I, a->w13, a->w2, w.yp,
+                                          w.h, w.err, ctr(w.err, CTR_FFN), s0, nullptr, nullptr,
+                                          nullptr, /*parts=*/2, nullptr, packed);
+        mark(5);
+        if (rc == MOE_OK && overlap && cudaStreamWaitEvent(s0, ev_shared, 0) != cudaSuccess)
+            rc = MOE_ERR_CUDA;
+        if (rc == MOE_OK)
+            rc = moe_launch::combine(w.yp, T * k, w.s2r, w.w, w.ysh, T, k, d, out, w.err, s0);
+        mark(6);
+        if (own_events)
+            for (int i = 0; i < n_ev; ++i) cudaEventDestroy(ev[i]);
+        return rc;
+    }
     if (overlap) {
         if (rc == MOE_OK && cudaStreamWaitEvent(s1, ev_start, 0) != cudaSuccess) rc = MOE_ERR_CUDA;
         if (rc == MOE_OK && zero_on_s1 &&
@@ -460,10 +528,8 @@ int moe_layer(const moe_layer_args* a, float* out, void* ws, size_t ws_bytes, vo
     if (rc == MOE_OK && !fused)
         rc = moe_launch::combine(w.yp, T * k, w.s2r, w.w, w.ysh, T, k, d, out, w.err, s0);
     mark(6);
-    if (own_events) {
-        cudaEventDestroy(ev_start);
-        cudaEventDestroy(ev_shared);
-    }
+    if (own_events)
+        for (int i = 0; i < n_ev; ++i) cudaEventDestroy(ev[i]);
     return rc;
 }
 

@@ -82,12 +82,15 @@ struct FusedCombine {
 };
 // parts: 1 = gate/up launch, 2 = down launch, 3 = both.  before_down: an
 // event the down launch waits for (e.g. the shared expert's gate/up on
-// another stream).
+// another stream).  heur_E: the expert count whose rows the launch's tile
+// choice averages over (0: E); a launch over a range of a layer's experts
+// passes the layer's, so that it takes the tile the whole layer would.
 int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
                      const void* w13, const void* w2, float* y, void* h, uint32_t* err,
                      unsigned* work, cudaStream_t s, cudaEvent_t between = nullptr,
                      const SharedExpert* sh = nullptr, const FusedCombine* fc = nullptr,
-                     int parts = 3, cudaEvent_t before_down = nullptr, bool packed = false);
+                     int parts = 3, cudaEvent_t before_down = nullptr, bool packed = false,
+                     int heur_E = 0);
 // Expert weights [E, rows, K] bf16 into the tile-major layout (pairs: the
 // down projection's), on stream s.  rows % 128 == 0 (pairs: % 256), K % 64 == 0.
 int pack_weights(const void* w, int E, int rows, int K, bool pairs, void* out, cudaStream_t s);
@@ -116,10 +119,14 @@ int topk(const float* scores, const float* bias, int T, const moe_route_cfg* cfg
          float* scores_out = nullptr);
 size_t dispatch_ws_bytes(int T, int k, int E);
 int lookback_probe(void* flags_zeroed, uint64_t limit_ns, uint32_t* err, cudaStream_t s);
-// w_slot/w_row (both or neither): also write each permuted row's gate weight
+// w_slot/w_row (both or neither): also write each permuted row's gate weight.
+// parts: 1 = count and scan only, 2 = permute only (after a count launch of
+// the same call, on the same workspace), 3 = both.  The permute moves only
+// the slots routed to experts [e_lo, e_hi) (e_hi < 0: all).
 int dispatch(const int32_t* idx, const void* x, int dtype, int T, int d, int k, int E, int32_t* counts,
              int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_token, void* x_perm, void* ws,
-             uint32_t* err, cudaStream_t s, const float* w_slot = nullptr, float* w_row = nullptr);
+             uint32_t* err, cudaStream_t s, const float* w_slot = nullptr, float* w_row = nullptr,
+             int parts = 3, int e_lo = 0, int e_hi = -1);
 size_t ffn_ws_bytes(int rows, int I, int dtype);
 int grouped_ffn(const void* x_perm, const int32_t* offsets, int E, int rows, int d, int I,
                 const void* w13, const void* w2, int dtype, float* y, void* h_ws, uint32_t* err,

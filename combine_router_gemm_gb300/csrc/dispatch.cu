@@ -224,13 +224,14 @@ __global__ void __launch_bounds__(256) permute_kernel(
     const int32_t* __restrict__ idx, const int* __restrict__ pos, const int32_t* __restrict__ offsets,
     int S, int k, int E, const uint4* __restrict__ x, int row_vecs, int32_t* __restrict__ slot_to_row,
     int32_t* __restrict__ row_to_token, uint4* __restrict__ x_perm, const float* __restrict__ w_slot,
-    float* __restrict__ w_row, const uint32_t* err) {
+    float* __restrict__ w_row, const uint32_t* err, int e_lo, int e_hi) {
     if (moe::read_error(err)) return;
     const int lane = threadIdx.x & 31;
     const int s = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (s >= S) return;
     const int e = idx[s];
     if (e < 0 || e >= E) return;  // already flagged by the count kernel
+    if (e < e_lo || e >= e_hi) return;  // another launch's expert range
     const int row = offsets[e] + pos[s];
     const int t = s / k;
     if (lane == 0) {
@@ -267,10 +268,22 @@ size_t dispatch_ws_bytes(int T, int k, int E) { return ws_bytes(T * k, E); }
 int dispatch(const int32_t* idx, const void* x, int dtype, int T, int d, int k, int E,
              int32_t* counts, int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_token,
              void* x_perm, void* ws, uint32_t* err, cudaStream_t s, const float* w_slot,
-             float* w_row) {
+             float* w_row, int parts, int e_lo, int e_hi) {
     const int S = T * k;
     const int nb = moe::ceil_div(S, DISP_CH);
     DispatchWs st = carve(ws, S, E);
+    if (e_hi < 0) e_hi = E;
+    if (parts & 2 && (e_lo < 0 || e_lo > e_hi || e_hi > E)) return MOE_ERR_INVALID_ARG;
+    if (!(parts & 1)) {
+        // the permute alone, after a count launch of the same call
+        if (!(parts & 2) || e_lo == e_hi) return MOE_OK;
+        const size_t esize = dtype == MOE_BF16 ? 2 : 4;
+        const int row_vecs = (int)((size_t)d * esize / 16);
+        permute_kernel<<<moe::ceil_div(S, 8), 256, 0, s>>>(
+            idx, st.pos, offsets, S, k, E, static_cast<const uint4*>(x), row_vecs, slot_to_row,
+            row_to_token, static_cast<uint4*>(x_perm), w_slot, w_row, err, e_lo, e_hi);
+        return moe_host::launch_status();
+    }
     if (cudaMemsetAsync(ws, 0, 16 + sizeof(int) * (size_t)nb, s) != cudaSuccess) return MOE_ERR_CUDA;
     const size_t smem = sizeof(int) * (size_t)(DISP_WARPS + 2) * E;
     if (smem > 48 * 1024 &&
@@ -279,12 +292,12 @@ int dispatch(const int32_t* idx, const void* x, int dtype, int T, int d, int k, 
         return MOE_ERR_CUDA;
     dispatch_count_kernel<<<nb, DISP_THREADS, smem, s>>>(idx, S, E, st, counts, offsets, err);
     int rc = moe_host::launch_status();
-    if (rc != MOE_OK) return rc;
+    if (rc != MOE_OK || !(parts & 2) || e_lo == e_hi) return rc;
     const size_t esize = dtype == MOE_BF16 ? 2 : 4;
     const int row_vecs = (int)((size_t)d * esize / 16);
     permute_kernel<<<moe::ceil_div(S, 8), 256, 0, s>>>(
         idx, st.pos, offsets, S, k, E, static_cast<const uint4*>(x), row_vecs, slot_to_row,
-        row_to_token, static_cast<uint4*>(x_perm), w_slot, w_row, err);
+        row_to_token, static_cast<uint4*>(x_perm), w_slot, w_row, err, e_lo, e_hi);
     return moe_host::launch_status();
 }
 

@@ -1713,8 +1713,9 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
                      const void* w13, const void* w2, float* y, void* h, uint32_t* err,
                      unsigned* work, cudaStream_t s, cudaEvent_t between,
                      const SharedExpert* sh, const FusedCombine* fc, int parts,
-                     cudaEvent_t before_down, bool packed) {
+                     cudaEvent_t before_down, bool packed, int heur_E) {
     if (E > MAX_E) return MOE_ERR_UNSUPPORTED;
+    const int HE = heur_E > 0 ? heur_E : E;  // experts the rows are averaged over
     CUtensorMap a1, a2, a1s, a2s;
     BMaps b1, b2, b1s, b2s;
     if (!make_weight_map(&a1, w13, (uint64_t)E * 2 * I, d, packed) ||
@@ -1752,11 +1753,11 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     //            stages, double-buffered), 2.85 ms with 256 (3 stages);
     //   down:    128 only below 32 rows per expert (decode), else 256
     //            (prefill: 1.57 ms vs 2.01 ms with 128).
-    const bool gu_wide = (long long)rows >= (long long)MOE_GU_WIDE_ROWS * E;
-    const bool dn_wide = (long long)rows >= (long long)MOE_DN_WIDE_ROWS * E;
+    const bool gu_wide = (long long)rows >= (long long)MOE_GU_WIDE_ROWS * HE;
+    const bool dn_wide = (long long)rows >= (long long)MOE_DN_WIDE_ROWS * HE;
     // a few rows per expert (decode): 32-token tiles, whose 36 KB stages let
     // each SM keep 6 weight-tile pairs in flight instead of 4
-    const bool narrow = MOE_NARROW_ROWS > 0 && (long long)rows < (long long)MOE_NARROW_ROWS * E;
+    const bool narrow = MOE_NARROW_ROWS > 0 && (long long)rows < (long long)MOE_NARROW_ROWS * HE;
     // a dense problem alone (offsets == NULL, no second problem): the unit
     // counts are known here
     const bool dense = offsets == nullptr;
@@ -1777,7 +1778,7 @@ int grouped_ffn_bf16(const void* x_perm, const int32_t* offsets, int E, int rows
     // MOE_QUAD_DN_ROWS rows per expert)
     const bool gu_quad = MOE_QUAD_GU && gu_pair && MOE_PAIR_GU_BN == 256 &&
                          pair_capacity<0, BN2, 4>() > 0;
-    const bool dn_quad = MOE_QUAD_DN && dn_pair && (long long)rows >= (long long)MOE_QUAD_DN_ROWS * E &&
+    const bool dn_quad = MOE_QUAD_DN && dn_pair && (long long)rows >= (long long)MOE_QUAD_DN_ROWS * HE &&
                          pair_capacity<1, BN2, 4>() > 0;
     // a dense problem alone: its units on pairs (256 features x 256 tokens for
     // gate/up, 512 x 256 for down), for the balanced grid

@@ -219,15 +219,16 @@ typedef struct {
     const void* w_router_split;
     /* optional: MOE_LAYER_SYNC_EVENTS cudaEvent_t handles (host array,
      * caller-created, timing disabled is best) with which the call forks
-     * stream2 from `stream` and joins it back.  NULL: the call creates and
-     * destroys two events itself, a host-side cost on every call.  A caller
-     * that reuses them must not record them elsewhere while a call that
-     * uses them is being enqueued. */
+     * stream2 from `stream` and joins it back (with MOE_LAYER_SPLIT_DISPATCH
+     * it reads all four; otherwise only the first two).  NULL: the call
+     * creates and destroys the events it needs itself, a host-side cost on
+     * every call.  A caller that reuses them must not record them elsewhere
+     * while a call that uses them is being enqueued. */
     void* const* sync_events;
 } moe_layer_args;
 
 /* Number of events in moe_layer_args.sync_events. */
-#define MOE_LAYER_SYNC_EVENTS 2
+#define MOE_LAYER_SYNC_EVENTS 4
 
 /* moe_layer_args.flags: add the down projection's results straight into `out`
  * (16-byte fp32 vector reductions in the grouped GEMM's epilogue) instead of
@@ -249,6 +250,17 @@ typedef struct {
  * expert's first GEMM ahead of the router GEMM and delay it.  Results are
  * the same either way. */
 #define MOE_LAYER_SHARED_AFTER_ROUTER 4
+
+/* moe_layer_args.flags: dispatch overlapped with the routed gate/up (the
+ * pages' two-stream dispatch overlap, CUCo, Table 4, row "MoE
+ * Dispatch/Combine", on one GPU).  After the count and scan, stream2
+ * permutes the tokens of experts [E/2, E) (then runs the shared expert, if
+ * any) while `stream` permutes those of experts [0, E/2) and runs their
+ * gate/up GEMM; the gate/up of the upper half follows once its permute is
+ * done, then the down projection over all experts and the combine.  Needs
+ * stream2, bf16 and no MOE_LAYER_FUSED_COMBINE (else MOE_ERR_UNSUPPORTED);
+ * E = 1 runs unsplit.  Results are the same, bit for bit, as without it. */
+#define MOE_LAYER_SPLIT_DISPATCH 8
 
 /* Source: the pages have no counterpart (sizing query).
  * Workspace bytes moe_layer needs (0 for invalid sizes or configuration).

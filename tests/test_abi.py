@@ -191,7 +191,27 @@ def test_layer_packed_flag_checks(lib):
         a = args(**bad)
         n = lib.moe_layer_workspace_size(ctypes.byref(a)) or need
         assert lib.moe_layer(ctypes.byref(a), P, P, n, None, None) == B.ERR_UNSUPPORTED, bad
-    assert lib.moe_layer(ctypes.byref(args(flags=8)), P, P, need, None, None) == B.ERR_INVALID_ARG
+    assert lib.moe_layer(ctypes.byref(args(flags=16)), P, P, need, None, None) == B.ERR_INVALID_ARG
+
+
+def test_layer_split_dispatch_checks(lib):
+    """The split dispatch needs a second stream, bf16 and the unfused
+    combine; each miss is refused on the host before anything is enqueued."""
+    def args(**kw):
+        a = dict(x=P, w_router=P, bias=None, w13=P, w2=P, w13_sh=None, w2_sh=None, T=64, d=256,
+                 I=256, I_sh=0, dtype=B.BF16, route=cfg(), scores_out=None, topk_idx_out=None,
+                 topk_w_out=None, offsets_out=None, flags=B.LAYER_SPLIT_DISPATCH)
+        a.update(kw)
+        return B.LayerArgs(**a)
+    need = lib.moe_layer_workspace_size(ctypes.byref(args()))
+    assert need > 0
+    s2 = ctypes.c_void_p(P)  # any non-null stream handle: refused before use
+    assert lib.moe_layer(ctypes.byref(args()), P, P, need, None, None) == B.ERR_UNSUPPORTED
+    assert lib.moe_layer(ctypes.byref(args()), P, P, need, s2, s2) == B.ERR_UNSUPPORTED
+    for bad in (dict(dtype=B.F32), dict(flags=B.LAYER_SPLIT_DISPATCH | B.LAYER_FUSED_COMBINE)):
+        a = args(**bad)
+        n = lib.moe_layer_workspace_size(ctypes.byref(a)) or need
+        assert lib.moe_layer(ctypes.byref(a), P, P, n, None, s2) == B.ERR_UNSUPPORTED, bad
 
 
 def test_split_router_weight_rejects(lib):

@@ -372,3 +372,64 @@ def test_layer_presplit_router_bit_identical():
     a, b = once.forward(inp["x"]), each.forward(inp["x"])
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+def _split_vs_plain(cfg, inp):
+    """The layer with the dispatch split over two streams and without it, on
+    the same weights and tokens: outputs, routing and offsets."""
+    args = (inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"], inp["w2_sh"],
+            B.cfg_from(cfg), cfg.T)
+    res = []
+    for split in (True, False):
+        layer = B.MoELayer(*args, split_dispatch=split)
+        assert (layer.stream2 is not None) or not split
+        idx, offs = cuda_i32((cfg.T, cfg.k)), cuda_i32(cfg.E + 1)
+        out = layer.forward(inp["x"], topk_idx_out=idx, offsets_out=offs)
+        rc, detail = B.moe_check_error(layer.ws)
+        assert rc == B.OK, detail
+        res.append((out, idx, offs))
+        del layer
+    torch.cuda.synchronize()
+    (a, ia, oa), (b, ib, ob) = res
+    assert torch.equal(ia, ib) and torch.equal(oa, ob)
+    assert torch.equal(a, b)
+    return a
+
+
+@pytest.mark.parametrize("cfg", SMALL_BF16, ids=lambda c: c.name)
+def test_layer_split_dispatch_bit_identical(cfg):
+    """The permute of the upper half of the experts on the second stream
+    beside the lower half's gate/up (then that half's gate/up): the same
+    output, bit for bit, as the one-pass dispatch."""
+    inp = inputs.make_inputs(cfg, seed=11, device="cuda")
+    _split_vs_plain(cfg, inp)
+
+
+def test_layer_split_dispatch_all_tokens(oracle):
+    cfg = SMALL_BF16[0]
+    inp = inputs.make_inputs(cfg, seed=12, device="cuda")
+    out = _split_vs_plain(cfg, inp)
+    sc, ridx, _, rout = oracle_tokens(oracle, cfg, inp, torch.arange(cfg.T, device="cuda"))
+    amb = near_tie_tokens(sc, np_(inp["bias"]), cfg.k, cfg.n_group, cfg.topk_group,
+                          abs_margin=router_margin(cfg, inp))
+    layer = B.MoELayer(inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"],
+                       inp["w2_sh"], B.cfg_from(cfg), cfg.T, split_dispatch=True)
+    idx = cuda_i32((cfg.T, cfg.k))
+    layer.forward(inp["x"], topk_idx_out=idx)
+    torch.cuda.synchronize()
+    same = (np_(idx) == ridx).all(1)
+    assert (same | amb).all()
+    assert_bf16_close(np_(out)[same], rout[same], "split dispatch")
+
+
+@pytest.mark.parametrize("name", ["mixtral_bf16", "dsv3_prefill", "dsv3_zipf"])
+def test_layer_split_dispatch_full_size_bit_identical(name):
+    """At full size (Zipf: uneven halves and empty experts; Mixtral: no
+    shared expert, the second stream free for the permute)."""
+    cfg = inputs.CONFIGS[name]
+    inp = inputs.make_inputs(cfg, seed=0, device="cuda")
+    out = _split_vs_plain(cfg, inp)
+    assert torch.isfinite(out).all()
+    del inp, out
+    gc.collect()
+    torch.cuda.empty_cache()
