@@ -290,15 +290,17 @@ def test_layer_fused_combine_full_size(oracle):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("cfg", [SMALL_BF16[0], SMALL_BF16[2], SMALL_BF16[3],
-                                 inputs.CONFIGS["tiny_fp32"]],
-                         ids=lambda c: c.name)
-def test_layer_cuda_graph_replay(oracle, cfg):
-    """The layer recorded into a CUDA graph (both streams) and replayed on new
-    tokens gives exactly what a direct call gives, and matches the oracle."""
+@pytest.mark.parametrize("cfg,split", [(SMALL_BF16[0], False), (SMALL_BF16[2], False),
+                                       (SMALL_BF16[3], False), (inputs.CONFIGS["tiny_fp32"], False),
+                                       (SMALL_BF16[0], True), (SMALL_BF16[1], True)],
+                         ids=lambda v: getattr(v, "name", "split" if v else "one-pass"))
+def test_layer_cuda_graph_replay(oracle, cfg, split):
+    """The layer recorded into a CUDA graph (both streams; also with the
+    dispatch split over them) and replayed on new tokens gives exactly what
+    a direct call gives, and matches the oracle."""
     inp = inputs.make_inputs(cfg, seed=4, device="cuda")
     layer = B.MoELayer(inp["w_router"], inp["bias"], inp["w13"], inp["w2"], inp["w13_sh"],
-                       inp["w2_sh"], B.cfg_from(cfg), cfg.T)
+                       inp["w2_sh"], B.cfg_from(cfg), cfg.T, split_dispatch=split)
     x = inp["x"].clone()
     graph, out = layer.capture(x)
     for seed in (5, 6):
