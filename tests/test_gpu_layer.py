@@ -435,3 +435,29 @@ def test_layer_split_dispatch_full_size_bit_identical(name):
     del inp, out
     gc.collect()
     torch.cuda.empty_cache()
+
+
+SPLIT_EDGE = [
+    # an odd expert count: halves of 2 and 3 experts
+    (inputs.MoEConfig("split_odd", T=333, d=256, E=5, k=2, I=128, dtype="bf16",
+                      expert_std=0.06), None),
+    (EDGE[0][0], None),  # a single token: one half gets at most 4 slots
+    (EDGE[1][0], None),  # E = 1: runs unsplit
+    # every token on experts of the upper half; the lower half's permute and
+    # gate/up launch have nothing to do, and the other experts' NaN weights
+    # must never be read
+    (EDGE[2][0], [17, 20, 25, 30]),
+]
+
+
+@pytest.mark.parametrize("cfg,forced", SPLIT_EDGE, ids=lambda v: getattr(v, "name", "f"))
+def test_layer_split_dispatch_edge_cases(cfg, forced):
+    inp = inputs.make_inputs(cfg, seed=13, device="cuda")
+    if forced is not None:
+        inp["bias"] = torch.full((cfg.E,), -5.0, device="cuda")
+        inp["bias"][forced] = 5.0
+        rest = [e for e in range(cfg.E) if e not in forced]
+        inp["w13"][rest] = float("nan")
+        inp["w2"][rest] = float("nan")
+    out = _split_vs_plain(cfg, inp)
+    assert torch.isfinite(out).all()
