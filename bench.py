@@ -61,16 +61,16 @@ NOMINAL_BF16_TFLOPS = 2250.0
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the routed
 # gate/up GEMM per launch, from ncu captures of this kernel source.  Reported
 # as null once the kernel source no longer matches the captured one.
-TRAFFIC = {"source_sha256": "a9eeb0ec0cc6e01b31a49ad3ea18fe4fae17e800cd1a1e71d5e5bd69acfb8863",
+TRAFFIC = {"source_sha256": "ef65fc98dbc776913c77b9a236bf365276ff464d7be7536a60a55f25aa034be4",
            # routed gate/up launch on tile-major weights (the shared expert
            # runs on the second stream): dsv3_prefill_e32 from an ncu capture
-           # of the 32-expert case (dram__bytes_read.sum 1.950768e9 +
-           # dram__bytes_write.sum 0.017970e9); dsv3_prefill is that capture
+           # of the 32-expert case (dram__bytes_read.sum 1.951280e9 +
+           # dram__bytes_write.sum 0.018274e9); dsv3_prefill is that capture
            # scaled by the units processed (8x the experts at the same rows
            # per expert, 8x the tokens), the workload being too large for a
            # multi-metric capture
-           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.968738e9,
-                                            "dsv3_prefill": 8 * 1.968738e9}}
+           "bytes_per_launch_at_workload": {"dsv3_prefill_e32": 1.969554e9,
+                                            "dsv3_prefill": 8 * 1.969554e9}}
 
 
 def peaks():
